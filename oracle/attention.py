@@ -1,0 +1,353 @@
+"""Oracle for exact tiled attention: plain, slow float64 NumPy on the CPU.
+
+TEST INFRASTRUCTURE.  Only the tests, the smoke check of ``__graft_entry__`` and
+the CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with the CUDA path and the CUDA path never calls it.
+
+Sources (three web pages on FlashAttention):
+  [p1] "CS349E lecture 11: 03_flash_backward.py" (functions std_fwd_bwd_io,
+       demo1_gradcheck, demo4_causal)
+  [p2] "CS324 lecture 8: 03_online_softmax_and_flash.py" (demo2_online,
+       demo3_forward, demo4_backward, flash_attention_torch)
+  [p3] "CS336 Assignment 2 notes: FlashAttention & DDP", Part 1:
+       §1.1 (standard attention), §1.2 (FlashAttention-2 forward),
+       §1.3 (Triton kernel: causal whole-tile skip), §1.4 (backward,
+       Equations 13-19, two-kernel backward)
+
+Functions and the pins that tie each to something other than itself (all in
+tests/test_oracle_pins.py):
+
+  standard_attention_fwd   plain definition of softmax(Q K^T s) V and its
+                           logsumexp.  Pinned by torch fp64 autograd and SDPA,
+                           the N=1 and equal-keys closed forms, and agreement
+                           with flash_forward_tiled.
+  standard_attention_bwd   plain softmax-Jacobian backward.  Pinned by central
+                           differences, torch fp64 autograd, and the identity
+                           sum_j P_ij dP_ij = rowsum(dO * O).
+  rows_fwd_bwd / key_rows_bwd
+                           the same definitions evaluated on a subset of query
+                           rows / key rows.  Pinned by equality with the full
+                           functions on small cases.
+  online_softmax           streaming (m, l) recurrence.  Pinned by the worked
+                           trace on x = [2,-1,3,0.5,6,1,-2,5.5], block 3.
+  flash_forward_tiled      FlashAttention-2 forward in the notes' order.
+  flash_backward_tiled     Equations 13-19 tile by tile, key/value tiles outer.
+  causal_tile_pairs        closed-form count of computed tile pairs.  Pinned by
+                           brute force and the fraction 1/2 + 1/(2T).
+
+Conventions: arrays are [..., N, d]; L is the natural-log logsumexp of the
+scaled scores (S already includes the scale); causal means query i sees keys
+0..i (top-left alignment).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+ROW_BLOCK = 256  # rows evaluated at a time, so no N x N array is ever held
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+def _heads(x: np.ndarray) -> np.ndarray:
+    """[..., N, d] -> [BH, N, d] view."""
+    return x.reshape((-1,) + x.shape[-2:])
+
+
+def _scale(d: int, scale) -> float:
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+def _scores(q_rows: np.ndarray, row_ids: np.ndarray, K: np.ndarray, causal: bool, s: float):
+    """Scaled scores of some query rows against all keys, masked when causal.
+
+    S = Q K^T / sqrt(d) ([p3] §1.4 Eq 13); a causal mask sets key j > query i
+    to -inf ([p2] flash_attention_torch, cols > rows).
+    """
+    S = (q_rows @ K.T) * s
+    if causal:
+        cols = np.arange(K.shape[0])[None, :]
+        S = np.where(cols > row_ids[:, None], -np.inf, S)
+    return S
+
+
+def _logsumexp_rows(S: np.ndarray) -> np.ndarray:
+    """Safe logsumexp per row: m + ln(sum exp(S - m)) ([p2] demo1_overflow; [p3] §1.2)."""
+    m = S.max(axis=1)
+    return m + np.log(np.exp(S - m[:, None]).sum(axis=1))
+
+
+# ---------------------------------------------------------------------------
+# Plain definition (no tiling, no online softmax)
+# ---------------------------------------------------------------------------
+
+def standard_attention_fwd(Q, K, V, causal: bool = False, scale=None):
+    """O = softmax(Q K^T s) V and L = logsumexp of each row of Q K^T s.
+
+    [p3] §1.1 (S = QK^T, P = softmax(S), O = PV) and §1.2 (L = m + log l).
+    Returns (O [..., N, d], L [..., N]) in float64.
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    lead, (N, d) = Q.shape[:-2], Q.shape[-2:]
+    s = _scale(d, scale)
+    Qh, Kh, Vh = _heads(Q), _heads(K), _heads(V)
+    O = np.empty(Qh.shape[:-1] + (Vh.shape[-1],))
+    L = np.empty(Qh.shape[:-1])
+    for h in range(Qh.shape[0]):
+        for r0 in range(0, N, ROW_BLOCK):
+            rows = np.arange(r0, min(N, r0 + ROW_BLOCK))
+            S = _scores(Qh[h, rows], rows, Kh[h], causal, s)
+            Lr = _logsumexp_rows(S)
+            P = np.exp(S - Lr[:, None])  # softmax of each row
+            O[h, rows] = P @ Vh[h]
+            L[h, rows] = Lr
+    return O.reshape(lead + O.shape[-2:]), L.reshape(lead + (N,))
+
+
+def standard_attention_bwd(Q, K, V, dO, causal: bool = False, scale=None):
+    """Gradients of sum(O * dO) with respect to Q, K, V (plain softmax backward).
+
+    P is formed from its definition; then ([p3] §1.4 Equations 15-19, and the
+    standard backward of [p1]/[p2] that uses the stored P):
+        dV = P^T dO,  dP = dO V^T,
+        D_i = sum_j P_ij dP_ij       (the softmax Jacobian term),
+        dS = P * (dP - D),  dQ = dS K s,  dK = dS^T Q s.
+    Returns (dQ, dK, dV, D) in float64.
+    """
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    lead, (N, d) = Q.shape[:-2], Q.shape[-2:]
+    s = _scale(d, scale)
+    Qh, Kh, Vh, dOh = _heads(Q), _heads(K), _heads(V), _heads(dO)
+    dQ = np.zeros_like(Qh)
+    dK = np.zeros_like(Kh)
+    dV = np.zeros_like(Vh)
+    D = np.empty(Qh.shape[:-1])
+    for h in range(Qh.shape[0]):
+        for r0 in range(0, N, ROW_BLOCK):
+            rows = np.arange(r0, min(N, r0 + ROW_BLOCK))
+            S = _scores(Qh[h, rows], rows, Kh[h], causal, s)
+            P = np.exp(S - _logsumexp_rows(S)[:, None])
+            dP = dOh[h, rows] @ Vh[h].T
+            Dr = (P * dP).sum(axis=1)
+            dS = P * (dP - Dr[:, None])
+            dQ[h, rows] = (dS @ Kh[h]) * s
+            dK[h] += (dS.T @ Qh[h, rows]) * s
+            dV[h] += P.T @ dOh[h, rows]
+            D[h, rows] = Dr
+    shp = lead + (N, d)
+    return (dQ.reshape(shp), dK.reshape(lead + Kh.shape[-2:]),
+            dV.reshape(lead + Vh.shape[-2:]), D.reshape(lead + (N,)))
+
+
+# ---------------------------------------------------------------------------
+# The same definitions on a subset of rows (for sequence lengths where the
+# full result is too slow on the CPU)
+# ---------------------------------------------------------------------------
+
+def rows_fwd_bwd(Q, K, V, dO, rows, causal: bool = False, scale=None):
+    """O, L, dQ and D of the given query rows of every head.
+
+    Each of these depends only on its own query row (plus all of K and V):
+    O_i = P_i V, L_i = logsumexp(S_i), D_i = sum_j P_ij dP_ij and
+    dQ_i = sum_j P_ij (dP_ij - D_i) K_j s.   Q, K, V, dO are [BH, N, d].
+    Returns arrays [BH, len(rows), ...].
+    """
+    Q, K, V, dO = _f64(Q), _f64(K), _f64(V), _f64(dO)
+    rows = np.asarray(rows)
+    d = Q.shape[-1]
+    s = _scale(d, scale)
+    BH = Q.shape[0]
+    O = np.empty((BH, len(rows), V.shape[-1]))
+    L = np.empty((BH, len(rows)))
+    dQ = np.empty((BH, len(rows), d))
+    D = np.empty((BH, len(rows)))
+    for h in range(BH):
+        for b0 in range(0, len(rows), ROW_BLOCK):
+            r = rows[b0:b0 + ROW_BLOCK]
+            S = _scores(Q[h, r], r, K[h], causal, s)
+            Lr = _logsumexp_rows(S)
+            P = np.exp(S - Lr[:, None])
+            dP = dO[h, r] @ V[h].T
+            Dr = (P * dP).sum(axis=1)
+            O[h, b0:b0 + len(r)] = P @ V[h]
+            L[h, b0:b0 + len(r)] = Lr
+            D[h, b0:b0 + len(r)] = Dr
+            dQ[h, b0:b0 + len(r)] = ((P * (dP - Dr[:, None])) @ K[h]) * s
+    return O, L, dQ, D
+
+
+def key_rows_bwd(Q, K, V, dO, L, D, keys, causal: bool = False, scale=None):
+    """dK and dV of the given key rows of every head, from full-length L and D.
+
+    dV_j = sum_i P_ij dO_i and dK_j = sum_i dS_ij Q_i s with
+    P_ij = exp(S_ij - L_i) ([p3] §1.4 Eq 14) and dS_ij = P_ij (dP_ij - D_i).
+    L and D ([BH, N]) must be the oracle's own (standard_attention_fwd /
+    rows_fwd_bwd over all rows).  Returns (dK, dV) as [BH, len(keys), d].
+    """
+    Q, K, V, dO, L, D = (_f64(x) for x in (Q, K, V, dO, L, D))
+    keys = np.asarray(keys)
+    N, d = Q.shape[-2:]
+    s = _scale(d, scale)
+    BH = Q.shape[0]
+    dK = np.zeros((BH, len(keys), d))
+    dV = np.zeros((BH, len(keys), V.shape[-1]))
+    for h in range(BH):
+        Kk, Vk = K[h, keys], V[h, keys]
+        for r0 in range(0, N, ROW_BLOCK):
+            rows = np.arange(r0, min(N, r0 + ROW_BLOCK))
+            S = (Q[h, rows] @ Kk.T) * s
+            if causal:
+                S = np.where(keys[None, :] > rows[:, None], -np.inf, S)
+            P = np.exp(S - L[h, rows][:, None])
+            dP = dO[h, rows] @ Vk.T
+            dS = P * (dP - D[h, rows][:, None])
+            dV[h] += P.T @ dO[h, rows]
+            dK[h] += (dS.T @ Q[h, rows]) * s
+    return dK, dV
+
+
+# ---------------------------------------------------------------------------
+# The method itself, step by step in the pages' order (CPU, float64)
+# ---------------------------------------------------------------------------
+
+def online_softmax(x, block: int):
+    """Streaming softmax that keeps only the running max m and denominator l.
+
+    [p2] demo2_online and [p3] §1.2: for each block, m_new = max(m, max(block)),
+    l <- l * exp(m - m_new) + sum(exp(block - m_new)), m <- m_new; at the end
+    softmax = exp(x - m) / l.  Returns (softmax, trace) where trace holds
+    (elements read so far, m, l) after each block.
+    """
+    x = _f64(x)
+    m, l = -np.inf, 0.0
+    trace = []
+    for start in range(0, x.size, block):
+        blk = x[start:start + block]
+        m_new = max(m, float(blk.max()))
+        corr = math.exp(m - m_new) if m != -np.inf else 0.0
+        l = l * corr + float(np.exp(blk - m_new).sum())
+        m = m_new
+        trace.append((min(start + block, x.size), m, l))
+    return np.exp(x - m) / l, trace
+
+
+def _tile_visible(q_first: int, q_last: int, k_first: int, causal: bool) -> bool:
+    """Causal whole-tile skip: a key tile whose first key lies after the tile's
+    last query row is never read ([p3] §1.3, k_start > q_end; [p2]
+    flash_attention_torch visits key blocks j0 < i0 + n_i)."""
+    return (not causal) or k_first <= q_last
+
+
+def flash_forward_tiled(Q, K, V, Br: int, Bc: int, causal: bool = False, scale=None):
+    """FlashAttention-2 forward with deferred normalisation, one head at a time.
+
+    [p3] §1.2: per query tile, m = -inf, l = 0, O = 0; per visible key tile
+    S = Q_i K_j^T s, m_new = max(m, rowmax S), P = exp(S - m_new),
+    l = exp(m - m_new) l + rowsum P, O = exp(m - m_new) O + P V_j, m = m_new;
+    finally O = O / l and L = m + log l.  Diagonal tiles get the in-tile mask.
+    Returns (O, L, tile pairs computed).
+    """
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    lead, (N, d) = Q.shape[:-2], Q.shape[-2:]
+    Nk = K.shape[-2]
+    s = _scale(d, scale)
+    Qh, Kh, Vh = _heads(Q), _heads(K), _heads(V)
+    O = np.empty(Qh.shape[:-1] + (Vh.shape[-1],))
+    L = np.empty(Qh.shape[:-1])
+    tiles = 0
+    for h in range(Qh.shape[0]):
+        for i0 in range(0, N, Br):
+            rows = np.arange(i0, min(N, i0 + Br))
+            m = np.full(len(rows), -np.inf)
+            l = np.zeros(len(rows))
+            acc = np.zeros((len(rows), Vh.shape[-1]))
+            for j0 in range(0, Nk, Bc):
+                if not _tile_visible(rows[0], rows[-1], j0, causal):
+                    continue
+                tiles += 1
+                cols = np.arange(j0, min(Nk, j0 + Bc))
+                S = (Qh[h, rows] @ Kh[h, cols].T) * s
+                if causal:
+                    S = np.where(cols[None, :] > rows[:, None], -np.inf, S)
+                m_new = np.maximum(m, S.max(axis=1))
+                # a row whose every key so far is masked keeps m = -inf; guard exp(-inf + inf)
+                safe = np.where(np.isfinite(m_new), m_new, 0.0)
+                P = np.exp(S - safe[:, None])
+                corr = np.where(np.isfinite(m), np.exp(m - safe), 0.0)
+                l = corr * l + P.sum(axis=1)
+                acc = corr[:, None] * acc + P @ Vh[h, cols]
+                m = m_new
+            O[h, rows] = acc / l[:, None]
+            L[h, rows] = m + np.log(l)
+    return O.reshape(lead + O.shape[-2:]), L.reshape(lead + (N,)), tiles
+
+
+def flash_backward_tiled(Q, K, V, O, dO, L, Br: int, Bc: int, causal: bool = False, scale=None):
+    """Recompute backward, key/value tiles in the outer loop, one head at a time.
+
+    D = rowsum(O * dO) once ([p3] §1.4 Eq 17; [p1] demo1_gradcheck), then per
+    visible tile pair ([p3] §1.4 Equations 13-19):
+        S = Q_i K_j^T s (13), P = exp(S - L_i) (14), dV_j += P^T dO_i (15),
+        dP = dO_i V_j^T (16), dS = P * (dP - D_i) (17), dQ_i += dS K_j s (18),
+        dK_j += dS^T Q_i s (19).
+    dQ_i collects contributions from every key tile, as kernel 1 of the
+    two-kernel backward would with atomics ([p3] §1.4).
+    Returns (dQ, dK, dV, D, tile pairs computed).
+    """
+    Q, K, V, O, dO, L = (_f64(x) for x in (Q, K, V, O, dO, L))
+    lead, (N, d) = Q.shape[:-2], Q.shape[-2:]
+    Nk = K.shape[-2]
+    s = _scale(d, scale)
+    Qh, Kh, Vh, Oh, dOh = (_heads(x) for x in (Q, K, V, O, dO))
+    Lh = L.reshape(-1, N)
+    Dh = (Oh * dOh).sum(axis=-1)
+    dQ = np.zeros_like(Qh)
+    dK = np.zeros_like(Kh)
+    dV = np.zeros_like(Vh)
+    tiles = 0
+    for h in range(Qh.shape[0]):
+        for j0 in range(0, Nk, Bc):
+            cols = np.arange(j0, min(Nk, j0 + Bc))
+            for i0 in range(0, N, Br):
+                rows = np.arange(i0, min(N, i0 + Br))
+                if not _tile_visible(rows[0], rows[-1], j0, causal):
+                    continue
+                tiles += 1
+                S = (Qh[h, rows] @ Kh[h, cols].T) * s
+                if causal:
+                    S = np.where(cols[None, :] > rows[:, None], -np.inf, S)
+                P = np.exp(S - Lh[h, rows][:, None])
+                dV[h, cols] += P.T @ dOh[h, rows]
+                dP = dOh[h, rows] @ Vh[h, cols].T
+                dS = P * (dP - Dh[h, rows][:, None])
+                dQ[h, rows] += (dS @ Kh[h, cols]) * s
+                dK[h, cols] += (dS.T @ Qh[h, rows]) * s
+    shp = lead + (N, d)
+    return (dQ.reshape(shp), dK.reshape(lead + Kh.shape[-2:]), dV.reshape(lead + Vh.shape[-2:]),
+            Dh.reshape(lead + (N,)), tiles)
+
+
+def causal_tile_pairs(N: int, Br: int, Bc: int, causal: bool, Nk: int | None = None) -> int:
+    """Number of (query tile, key tile) pairs a tiled pass computes, per head.
+
+    Without the mask every pair: ceil(N/Br) * ceil(Nk/Bc).  With it, query tile
+    i sees key tiles 0 .. floor((min((i+1) Br, N) - 1) / Bc); for square tiles
+    and N a multiple of the tile this is T(T+1)/2, a fraction 1/2 + 1/(2T) of
+    all pairs ([p1] demo4_causal).
+    """
+    Nk = N if Nk is None else Nk
+    Tq, Tk = -(-N // Br), -(-Nk // Bc)
+    if not causal:
+        return Tq * Tk
+    return sum(min(Tk, (min((i + 1) * Br, N) - 1) // Bc + 1) for i in range(Tq))
+
+
+def attention_flops(N: int, d: int, causal: bool, B: int = 1, H: int = 1):
+    """Counted matmul FLOPs: 4 N^2 d forward and 10 N^2 d backward per head
+    (two and five N x N x d products at 2 flops per multiply-add; [p1]
+    std_fwd_bwd_io and demo3 observations), halved under the causal mask."""
+    f = 0.5 if causal else 1.0
+    return 4.0 * B * H * N * N * d * f, 10.0 * B * H * N * N * d * f
