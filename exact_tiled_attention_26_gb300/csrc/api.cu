@@ -1,0 +1,259 @@
+// C ABI of the exact tiled attention library: argument validation, tensor-map
+// encoding and launch of the kernels in fwd.cu, bwd.cu and aux.cu.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace fa {
+
+// One status word per device: kernels that give up on a wait record a site
+// code here (first writer wins); launches skip their work while it is set.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+std::mutex g_mu;
+unsigned long long* g_tile_counter = nullptr;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn get_encode() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_encode;
+}
+
+CUtensorMapSwizzle swizzle_for(int inner_bytes) {
+  switch (inner_bytes) {
+    case 128: return CU_TENSOR_MAP_SWIZZLE_128B;
+    case 64: return CU_TENSOR_MAP_SWIZZLE_64B;
+    case 32: return CU_TENSOR_MAP_SWIZZLE_32B;
+    default: return CU_TENSOR_MAP_SWIZZLE_NONE;
+  }
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Shape checks shared by every entry point; *empty is set when there is no work.
+fa_status check_shape(int B, int H, int N, int d, bool* empty) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long bh = static_cast<long long>(B) * H;
+  *empty = (bh == 0 || N == 0);
+  if (*empty) return FA_OK;
+  if (bh > 65535) return FA_ERR_UNSUPPORTED;
+  // element offsets are formed in 64 bits; keep rows within int range for tile indices
+  if (static_cast<long long>(N) > (1LL << 30)) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+bool check_scale(float scale) { return std::isfinite(scale) && scale > 0.f; }
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+}  // namespace
+
+int* device_status_word() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool encode_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int BH, int inner, int rows) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(inner), static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(inner * 2), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_bf16_2d(CUtensorMap* map, const void* base, int inner_total, int rows_total, int box_inner,
+                    int box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner_total), static_cast<cuuint64_t>(rows_total)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner_total) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  std::memset(map, 0, sizeof(*map));
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_inner * 2), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+fa_status fa_get_tile_config(int d, int pass, int* Br, int* Bc) {
+  if (Br == nullptr || Bc == nullptr) return FA_ERR_INVALID_ARG;
+  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (pass == 0) {
+    *Br = kFwdBr;
+    *Bc = kFwdBc;
+  } else if (pass == 1) {
+    *Br = bwd_br(d);
+    *Bc = kBwdBc;
+  } else {
+    return FA_ERR_INVALID_ARG;
+  }
+  return FA_OK;
+}
+
+long long fa_tile_pairs(int N, int d, int causal, int pass) {
+  int Br = 0, Bc = 0;
+  if (N < 0 || fa_get_tile_config(d, pass, &Br, &Bc) != FA_OK) return -1;
+  if (N == 0) return 0;
+  const long long Tq = (N + Br - 1) / Br, Tk = (N + Bc - 1) / Bc;
+  if (!causal) return Tq * Tk;
+  long long n = 0;
+  for (long long i = 0; i < Tq; ++i) {
+    const long long last = ((i + 1) * Br < N ? (i + 1) * Br : N) - 1;
+    const long long k = last / Bc + 1;
+    n += k < Tk ? k : Tk;
+  }
+  return n;
+}
+
+fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter) {
+  g_tile_counter = dev_counter;
+  return FA_OK;
+}
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
+                 int causal, float scale, fa_stream_t stream) {
+  bool empty = false;
+  fa_status st = check_shape(B, H, N, d, &empty);
+  if (st != FA_OK) return st;
+  if (!check_scale(scale)) return FA_ERR_INVALID_ARG;
+  if (empty) return FA_OK;
+  if (!Q || !K || !V || !O || !L) return FA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(L, 4))
+    return FA_ERR_INVALID_ARG;
+  int* status = device_status_word();
+  if (status == nullptr) return FA_ERR_CUDA;
+  FwdLaunch a{Q, K, V, O, L, B * H, N, d, causal ? 1 : 0, scale, stream, status, g_tile_counter};
+  return launch_fwd(a);
+}
+
+fa_status fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int H, int N, int d,
+                            fa_stream_t stream) {
+  bool empty = false;
+  fa_status st = check_shape(B, H, N, d, &empty);
+  if (st != FA_OK) return st;
+  if (empty) return FA_OK;
+  if (!O || !dO || !D) return FA_ERR_INVALID_ARG;
+  if (!aligned(O, 16) || !aligned(dO, 16) || !aligned(D, 4)) return FA_ERR_INVALID_ARG;
+  return launch_preprocess(O, dO, D, static_cast<long long>(B) * H * N, d, stream);
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
+  (void)causal;
+  bool empty = false;
+  if (check_shape(B, H, N, d, &empty) != FA_OK) return static_cast<size_t>(-1);
+  if (empty) return 0;
+  return static_cast<size_t>(B) * H * N * d * sizeof(float);
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
+                 const float* D, void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
+                 void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  bool empty = false;
+  fa_status st = check_shape(B, H, N, d, &empty);
+  if (st != FA_OK) return st;
+  if (!check_scale(scale)) return FA_ERR_INVALID_ARG;
+  if (empty) return FA_OK;
+  (void)O;  // O enters only through D = rowsum(dO * O), formed by fa_bwd_preprocess
+  if (!Q || !K || !V || !dO || !L || !D || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) || !aligned(dQ, 16) ||
+      !aligned(dK, 16) || !aligned(dV, 16) || !aligned(L, 4) || !aligned(D, 4))
+    return FA_ERR_INVALID_ARG;
+  const size_t need = fa_bwd_workspace_size(B, H, N, d, causal);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return FA_ERR_WORKSPACE;
+  int* status = device_status_word();
+  if (status == nullptr) return FA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, need, stream) != cudaSuccess) return FA_ERR_CUDA;
+  BwdLaunch a{Q, K, V, dO, L, D, static_cast<float*>(workspace), dK, dV, B * H, N, d, causal ? 1 : 0, scale,
+              stream, status, g_tile_counter};
+  st = launch_bwd(a);
+  if (st != FA_OK) return st;
+  return launch_dq_convert(static_cast<const float*>(workspace), dQ, static_cast<long long>(B) * H * N * d, stream);
+}
+
+fa_status fa_poll_device_error(fa_stream_t stream, int* detail) {
+  if (detail) *detail = 0;
+  int* status = device_status_word();
+  if (status == nullptr) return FA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FA_ERR_CUDA;
+  if (v == 0) return FA_OK;
+  const int zero = 0;
+  if (cudaMemcpy(status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FA_ERR_CUDA;
+  if (detail) *detail = v;
+  return FA_ERR_TIMEOUT;
+}
+
+fa_status fa_debug_timeout_probe(int limit_us, fa_stream_t stream) {
+  if (limit_us < 1 || limit_us > 1000000) return FA_ERR_INVALID_ARG;
+  int* status = device_status_word();
+  if (status == nullptr) return FA_ERR_CUDA;
+  return launch_timeout_probe(limit_us, stream, status);
+}
+
+fa_status fa_selftest_umma(int mode, const void* A, const void* B, float* C, int K, int N, fa_stream_t stream) {
+  if (mode < 0 || mode > 4) return FA_ERR_INVALID_ARG;
+  if ((K != 32 && K != 64 && K != 128) || (N != 32 && N != 64 && N != 128)) return FA_ERR_INVALID_ARG;
+  if (!A || !B || !C || !aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return FA_ERR_INVALID_ARG;
+  int* status = device_status_word();
+  if (status == nullptr) return FA_ERR_CUDA;
+  return launch_selftest(mode, A, B, C, K, N, stream, status);
+}
+
+}  // extern "C"

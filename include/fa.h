@@ -1,0 +1,169 @@
+/*
+ * Exact tiled attention (FlashAttention-2 forward and recompute backward) for
+ * NVIDIA GB300 (sm_103a): the C ABI of libfa_gb300.so.
+ *
+ * What is computed (sources: "CS336 Assignment 2 notes: FlashAttention & DDP",
+ * Part 1 §1.2-§1.4; "CS324 lecture 8: 03_online_softmax_and_flash.py";
+ * "CS349E lecture 11: 03_flash_backward.py"):
+ *
+ *   S = Q K^T * scale, P = softmax(S) row by row, O = P V          (§1.1, §1.2)
+ *   L = m + ln(l): the natural-log logsumexp of each row of S        (§1.2)
+ *   D = rowsum(dO * O)                                               (§1.4 Eq 17)
+ *   P = exp(S - L), dV = P^T dO, dP = dO V^T, dS = P * (dP - D),
+ *   dQ = dS K * scale, dK = dS^T Q * scale                           (§1.4 Eq 13-19)
+ *
+ * With `causal` != 0, query row i sees keys 0..i (top-left alignment) and a
+ * key tile whose first key lies after a query tile's last row is skipped
+ * entirely (§1.3; CS349E lecture 11 demo4_causal).
+ *
+ * Common conventions for every entry point below:
+ *   - Q, K, V, O, dO, dQ, dK, dV are bf16 (__nv_bfloat16) device arrays laid
+ *     out contiguously as [B, H, N, d] (row stride d elements).  L and D are
+ *     fp32 device arrays [B, H, N].  Every pointer must be 16-byte aligned
+ *     (L and D: 4-byte aligned).
+ *   - d must be 32, 64 or 128; B, H, N >= 0 and B*H <= 65535.  A call with
+ *     B*H*N == 0 does nothing and returns FA_OK (pointers may then be NULL).
+ *   - scale must be finite and > 0 (normally 1/sqrt(d)).
+ *   - The caller owns every buffer.  The library allocates no device memory.
+ *   - All work is enqueued asynchronously on `stream` (NULL = the legacy
+ *     default stream); entry points return after launch.  Argument errors are
+ *     reported before anything is enqueued; a failed launch returns
+ *     FA_ERR_CUDA.  Kernels never trap: each wait inside a kernel has a time
+ *     limit, and on expiry the kernel records an error in a device status word
+ *     and exits; fa_poll_device_error() reads it.
+ *   - No N x N buffer is ever allocated or written.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* fa_stream_t;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size or scale       */
+    FA_ERR_UNSUPPORTED = 2,  /* d not in {32,64,128}, B*H too large, no sm_103a  */
+    FA_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed                */
+    FA_ERR_TIMEOUT = 4,      /* a kernel gave up waiting (see fa_poll_device_error) */
+    FA_ERR_WORKSPACE = 5     /* workspace missing or smaller than required       */
+} fa_status;
+
+/*
+ * Forward pass: O = softmax(Q K^T * scale) V and L = logsumexp of each score row.
+ * "CS336 Assignment 2 notes" §1.2 (FlashAttention-2 forward: per query tile,
+ * running max m, running sum l, deferred normalisation O/l, L = m + log l)
+ * and §1.3 (whole-tile causal skip).
+ *   Q, K, V : in,  bf16 [B,H,N,d]
+ *   O       : out, bf16 [B,H,N,d]
+ *   L       : out, fp32 [B,H,N], natural log, in units of the scaled scores
+ */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
+                 int B, int H, int N, int d, int causal, float scale, fa_stream_t stream);
+
+/*
+ * Backward preprocessing: D_i = sum_k dO_ik * O_ik (fp32 accumulation).
+ * "CS336 Assignment 2 notes" §1.4 Eq 17 (D = rowsum(O * dO)); the identity
+ * D_i = sum_j dP_ij P_ij that lets D be formed once before the backward is
+ * the one of "CS349E lecture 11" demo1_gradcheck.
+ *   O, dO : in,  bf16 [B,H,N,d]
+ *   D     : out, fp32 [B,H,N]
+ */
+fa_status fa_bwd_preprocess(const void* O, const void* dO, float* D,
+                            int B, int H, int N, int d, fa_stream_t stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: an fp32 [B,H,N,d] accumulator for
+ * dQ (key tiles add their dS K contributions into it).  0 for empty inputs;
+ * (size_t)-1 for invalid sizes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal);
+
+/*
+ * Backward pass from the saved O and L: dQ, dK, dV.
+ * "CS336 Assignment 2 notes" §1.4 Equations 13-19, key/value tiles in the
+ * outer loop (kernel 1 of the notes' two-kernel backward) with dQ accumulated
+ * across key tiles in the fp32 workspace, then rounded to bf16.
+ *   Q, K, V, O, dO : in,  bf16 [B,H,N,d]
+ *   L              : in,  fp32 [B,H,N]  (from fa_fwd)
+ *   D              : in,  fp32 [B,H,N]  (from fa_bwd_preprocess)
+ *   dQ, dK, dV     : out, bf16 [B,H,N,d]
+ *   workspace      : scratch, >= fa_bwd_workspace_size() bytes, 16-byte
+ *                    aligned; overwritten (zeroed first) on every call, so
+ *                    calls that overlap on the GPU must not share it.
+ */
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* L, const float* D, void* dQ, void* dK, void* dV,
+                 int B, int H, int N, int d, int causal, float scale,
+                 void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * Tile shape used by a pass: pass 0 = forward (Br query rows x Bc keys),
+ * pass 1 = backward main kernel (Br query rows per inner step x Bc keys per
+ * CTA).  Host only; needs no GPU.
+ */
+fa_status fa_get_tile_config(int d, int pass, int* Br, int* Bc);
+
+/*
+ * Number of (query tile, key tile) pairs one head computes in a pass, from
+ * the closed form for the tiles of fa_get_tile_config (with the causal mask:
+ * query tile i sees key tiles 0 .. floor((min((i+1) Br, N) - 1) / Bc);
+ * "CS349E lecture 11" demo4_causal).  Host only; -1 on bad arguments.
+ */
+long long fa_tile_pairs(int N, int d, int causal, int pass);
+
+/*
+ * Debug: when `dev_counter` is non-NULL, every later fa_fwd / fa_bwd launch
+ * adds the number of tile pairs it computed to *dev_counter (a device
+ * unsigned long long the caller owns and zeroes).  NULL switches it off.
+ * Process-wide setting.
+ */
+fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  FA_OK if no kernel has given up since the last poll;
+ * FA_ERR_TIMEOUT otherwise, with the failing wait site in *detail (may be NULL).
+ * While the word is set, later launches skip their work.
+ */
+fa_status fa_poll_device_error(fa_stream_t stream, int* detail);
+
+/*
+ * Diagnostic: runs one wait on a barrier that nothing ever completes, with a
+ * limit of `limit_us` microseconds (1..1000000), on `stream`.  The kernel
+ * must give up, record FA_ERR_TIMEOUT and exit; a following
+ * fa_poll_device_error() returns it.  Exercises the bounded-wait path that
+ * every kernel uses, without faulting or hanging the GPU.
+ */
+fa_status fa_debug_timeout_probe(int limit_us, fa_stream_t stream);
+
+/*
+ * Diagnostic: one 128 x N x K tile product on the tensor cores through the
+ * same shared-memory / tensor-memory operand paths the attention kernels use.
+ *   mode 0: C = A B^T, A [128][K], B [N][K]          (both K-major)
+ *   mode 1: C = A B,   A [128][K], B [K][N]          (B N-major)
+ *   mode 2: C = A B,   A [128][K] staged in tensor memory, B [K][N]
+ *   mode 3: C = A^T B^T, A [K][128], B [N][K]        (A M-major)
+ *   mode 4: C = A^T B, A [K][128], B [K][N]          (both M/N-major)
+ * A, B: bf16 device arrays (row-major as shown); C: fp32 [128][N] device.
+ * K and N in {32, 64, 128}.  Not part of attention; used by the tests.
+ */
+fa_status fa_selftest_umma(int mode, const void* A, const void* B, float* C, int K, int N,
+                           fa_stream_t stream);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

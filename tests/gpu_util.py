@@ -1,0 +1,100 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the C ABI and
+compare with the float64 oracle on the same seeded bf16 inputs.
+
+Tolerances (element-wise against the oracle run on the bf16-rounded inputs):
+  O:  max |err| <= 1e-2 and ||err||_F / ||ref||_F <= 5e-3
+  L:  max |err| <= 2e-3
+  dQ, dK, dV: ||err||_F / ||ref||_F <= 1e-2
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import seeded_inputs as si
+
+TOL_O_ABS, TOL_O_REL, TOL_L_ABS, TOL_G_REL = 1e-2, 5e-3, 2e-3, 1e-2
+
+
+def rel_frob(got, ref):
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def lib():
+    """The binding; imported here so that collecting GPU tests on a machine
+    without the built library does not fail (they are skipped there)."""
+    import exact_tiled_attention_26_gb300 as fa
+    return fa
+
+
+def run_gpu(Q, K, V, dO, causal, scale=None, counter=False):
+    """Forward + preprocess + backward through the C ABI.  Inputs: bf16 CPU tensors
+    [B,H,N,d].  Returns CPU tensors and (if asked) the tile-pair counts."""
+    fa = lib()
+    B, H, N, d = Q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    dev = torch.device("cuda")
+    q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    D = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d, causal)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    cnt = torch.zeros(2, dtype=torch.int64, device=dev)
+    s = stream()
+    if counter:
+        fa.check(fa.fa_debug_set_tile_counter(cnt.data_ptr()))
+    try:
+        fa.check(fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+                           causal, scale, s), "fa_fwd")
+        if counter:
+            fa.check(fa.fa_debug_set_tile_counter(cnt.data_ptr() + 8))
+        fa.check(fa.fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), D.data_ptr(), B, H, N, d, s), "preprocess")
+        fa.check(fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                           D.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, causal, scale,
+                           ws.data_ptr(), ws.numel(), s), "fa_bwd")
+    finally:
+        if counter:
+            fa.fa_debug_set_tile_counter(None)
+    st, detail = fa.fa_poll_device_error(s)
+    fa.check(st, f"device status word (site {detail:#x})")
+    out = {"O": o, "L": lse, "D": D, "dQ": dq, "dK": dk, "dV": dv}
+    out = {n: t.cpu() for n, t in out.items()}
+    if counter:
+        out["tiles"] = cnt.cpu().tolist()
+    return out
+
+
+def assert_close(got: dict, ref: dict, label=""):
+    """got/ref: dicts of float64 arrays with keys among O, L, dQ, dK, dV."""
+    msgs = []
+    errs = {}
+    if "O" in ref:
+        ea, er = float(np.abs(got["O"] - ref["O"]).max()), rel_frob(got["O"], ref["O"])
+        errs["O"] = (ea, er)
+        if not (ea <= TOL_O_ABS and er <= TOL_O_REL):
+            msgs.append(f"O max-abs {ea:.3e} rel {er:.3e}")
+    if "L" in ref:
+        ea = float(np.abs(got["L"] - ref["L"]).max())
+        errs["L"] = ea
+        if not ea <= TOL_L_ABS:
+            msgs.append(f"L max-abs {ea:.3e}")
+    for n in ("dQ", "dK", "dV"):
+        if n in ref:
+            er = rel_frob(got[n], ref[n])
+            errs[n] = er
+            if not er <= TOL_G_REL:
+                msgs.append(f"{n} rel {er:.3e}")
+    assert not msgs, f"{label}: " + "; ".join(msgs)
+    return errs
+
+
+def f64(t):
+    return si.to_f64(t)

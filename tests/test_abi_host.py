@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports every
+symbol include/fa.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("fa_fwd", "fa_bwd_preprocess", "fa_bwd", "fa_bwd_workspace_size", "fa_status_string",
+              "fa_poll_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fa_lib):
+    lib = ctypes.CDLL(fa_lib.lib_path)
+    for n in _declared():
+        assert hasattr(lib, n), n
+    nm = subprocess.run(["nm", "-D", "--defined-only", fa_lib.lib_path], capture_output=True, text=True)
+    if nm.returncode == 0:
+        exported = set(re.findall(r" T (fa_[a-z0-9_]+)$", nm.stdout, flags=re.M))
+        assert set(_declared()) <= exported
+
+
+def test_binding_names_match_header(fa_lib):
+    for n in _declared():
+        assert hasattr(fa_lib, n), n
+
+
+def test_status_strings(fa_lib):
+    assert fa_lib.fa_status_string(fa_lib.FA_OK) == "FA_OK"
+    assert fa_lib.fa_status_string(fa_lib.FA_ERR_TIMEOUT) == "FA_ERR_TIMEOUT"
+    assert fa_lib.fa_status_string(99) == "FA_ERR_UNKNOWN"
+    assert fa_lib.fa_version() >= 100
+
+
+def test_argument_errors_before_any_cuda_call(fa_lib):
+    fa = fa_lib
+    p = 4096  # a 16-byte aligned fake address: never dereferenced, validation fails first
+    # unsupported head size
+    assert fa.fa_fwd(p, p, p, p, p, 1, 1, 64, 48, 0, 0.1, None) == fa.FA_ERR_UNSUPPORTED
+    # null pointers
+    assert fa.fa_fwd(None, p, p, p, p, 1, 1, 64, 64, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
+    # misaligned pointer
+    assert fa.fa_fwd(p + 2, p, p, p, p, 1, 1, 64, 64, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
+    # bad scale
+    for sc in (0.0, -1.0, float("inf"), float("nan")):
+        assert fa.fa_fwd(p, p, p, p, p, 1, 1, 64, 64, 0, sc, None) == fa.FA_ERR_INVALID_ARG
+    # negative sizes, too many heads
+    assert fa.fa_fwd(p, p, p, p, p, -1, 1, 64, 64, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd(p, p, p, p, p, 1024, 1024, 64, 64, 0, 0.1, None) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd_preprocess(None, p, p, 1, 1, 8, 32, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd(p, p, p, p, p, p, p, p, p, p, 1, 1, 64, 64, 1, 0.1, None, 0, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd(p, p, p, p, p, p, p, p, p, p, 1, 1, 64, 64, 1, 0.1, p, 100, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_debug_timeout_probe(0, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_selftest_umma(7, p, p, p, 64, 64, None) == fa.FA_ERR_INVALID_ARG
+
+
+def test_empty_inputs_are_no_ops(fa_lib):
+    fa = fa_lib
+    assert fa.fa_fwd(None, None, None, None, None, 0, 4, 128, 64, 1, 0.125, None) == fa.FA_OK
+    assert fa.fa_fwd(None, None, None, None, None, 2, 4, 0, 64, 0, 0.125, None) == fa.FA_OK
+    assert fa.fa_bwd_preprocess(None, None, None, 1, 1, 0, 128, None) == fa.FA_OK
+    assert fa.fa_bwd(*([None] * 10), 1, 1, 0, 128, 1, 0.1, None, 0, None) == fa.FA_OK
+    assert fa.fa_bwd_workspace_size(1, 1, 0, 128, 1) == 0
+
+
+def test_workspace_size(fa_lib):
+    assert fa_lib.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 2 * 16 * 4096 * 128 * 4
+    assert fa_lib.fa_bwd_workspace_size(1, 1, 10, 48, 0) == ctypes.c_size_t(-1).value
+
+
+def test_tile_config(fa_lib):
+    assert fa_lib.fa_get_tile_config(128, 0) == (0, 128, 128)
+    assert fa_lib.fa_get_tile_config(128, 1) == (0, 64, 128)
+    assert fa_lib.fa_get_tile_config(64, 1) == (0, 128, 128)
+    assert fa_lib.fa_get_tile_config(32, 1) == (0, 128, 128)
+    assert fa_lib.fa_get_tile_config(100, 0)[0] == fa_lib.FA_ERR_UNSUPPORTED
+    assert fa_lib.fa_get_tile_config(128, 2)[0] == fa_lib.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("N", [1, 63, 64, 127, 128, 129, 256, 1000, 1024, 4096, 8192, 32768])
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_tile_pair_counts_match_closed_form(fa_lib, N, d):
+    """The library's host count of tile pairs equals the oracle's closed form for
+    the kernel's own tiles (the forward: query tile outer; the backward: key tile
+    outer — the same set of visible pairs)."""
+    for pass_ in (0, 1):
+        _, br, bc = fa_lib.fa_get_tile_config(d, pass_)
+        for causal in (False, True):
+            assert fa_lib.fa_tile_pairs(N, d, causal, pass_) == oracle.causal_tile_pairs(N, br, bc, causal)
+
+
+def test_tile_pair_counts_for_the_workloads(fa_lib):
+    # 128 x 128 forward tiles: T(T+1)/2 of T^2 with the causal mask
+    for N, pairs in ((1024, 36), (4096, 528), (8192, 2080), (32768, 32896)):
+        assert fa_lib.fa_tile_pairs(N, 128, True, 0) == pairs
+        T = N // 128
+        assert fa_lib.fa_tile_pairs(N, 128, False, 0) == T * T
