@@ -1,0 +1,376 @@
+"""Benchmark of exact tiled attention, forward + backward, on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--quick]
+
+One step = the whole hot path on one batch: fa_fwd (O, L), fa_bwd_preprocess (D)
+and fa_bwd (dQ, dK, dV), all through the C ABI.  The default workload is the
+very-long-context shape B=1, H=32, N=32768, d=128, causal (its bf16 inputs,
+1 GiB, exceed the 129 MB L2, so no flush is needed between steps).  Throughput
+counts 4 N^2 d (forward) + 10 N^2 d (backward) FLOPs per head, halved with the
+causal mask.  Prints ONE JSON line (rank 0).
+
+--impl reference times the float64 CPU oracle instead (a deliberately slow
+program, run as it stands on the host cores, each step a bounded sample of the
+same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+HEADLINE = "vlong_1x32x32768x128"
+METRIC = "attention fwd+bwd TFLOP/s (bf16, d=128, N=4K-32K)"
+UNIT = "TFLOP/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------ clocks sampling
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[4:]))
+                except ValueError:
+                    continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        pmax = max(r[2] for r in rows)
+        loaded = [r for r in rows if r[2] >= 0.5 * pmax] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i, v in enumerate(r[3][1:5]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": pmax, "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------ our arm
+
+class Runner:
+    """Device buffers and the three C-ABI calls of one step."""
+
+    def __init__(self, fa, torch, w: si.Workload, causal: bool, dev):
+        self.fa, self.torch, self.w, self.causal = fa, torch, w, causal
+        Q, K, V, dO = si.make_workload(w)
+        self.host_in = [t.pin_memory() for t in (Q, K, V, dO)]
+        self.q, self.k, self.v, self.do = (t.to(dev, non_blocking=False) for t in self.host_in)
+        B, H, N, d = w.B, w.H, w.N, w.d
+        self.o = torch.empty_like(self.q)
+        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.D = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
+        self.ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d, causal)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+        self.s = self.stream.cuda_stream
+        self.scale = w.scale
+
+    def fwd(self):
+        w, fa = self.w, self.fa
+        fa.check(fa.fa_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(), self.o.data_ptr(),
+                           self.lse.data_ptr(), w.B, w.H, w.N, w.d, self.causal, self.scale, self.s), "fa_fwd")
+
+    def bwd(self):
+        w, fa = self.w, self.fa
+        fa.check(fa.fa_bwd_preprocess(self.o.data_ptr(), self.do.data_ptr(), self.D.data_ptr(), w.B, w.H, w.N, w.d,
+                                      self.s), "fa_bwd_preprocess")
+        fa.check(fa.fa_bwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(), self.o.data_ptr(),
+                           self.do.data_ptr(), self.lse.data_ptr(), self.D.data_ptr(), self.dq.data_ptr(),
+                           self.dk.data_ptr(), self.dv.data_ptr(), w.B, w.H, w.N, w.d, self.causal, self.scale,
+                           self.ws.data_ptr(), self.ws_bytes, self.s), "fa_bwd")
+
+    # kernels this library launches per step: fwd, preprocess, bwd main, dQ convert
+    LAUNCHES_PER_STEP = 4
+
+
+def time_steps(torch, r: Runner, steps: int, warmup: int, flush=None):
+    """Times K steps with CUDA events on the launching stream.  Returns per-phase
+    milliseconds (totals over the K steps)."""
+    for _ in range(warmup):
+        r.fwd()
+        r.bwd()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush()
+        ev[i][0].record(r.stream)
+        r.fwd()
+        ev[i][1].record(r.stream)
+        r.bwd()
+        ev[i][2].record(r.stream)
+    torch.cuda.synchronize()
+    fwd = sum(e[0].elapsed_time(e[1]) for e in ev)
+    bwd = sum(e[1].elapsed_time(e[2]) for e in ev)
+    return fwd, bwd
+
+
+def e2e_steps(torch, r: Runner, steps: int):
+    """Same step through the C ABI with host buffers: pinned host -> device copies of
+    Q, K, V, dO and device -> pinned host copies of O, L, dQ, dK, dV inside the timed region."""
+    outs = [r.o, r.lse, r.dq, r.dk, r.dv]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in r.host_in)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    dev_in = [r.q, r.k, r.v, r.do]
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(r.stream)
+    for _ in range(steps):
+        for d_, h_ in zip(dev_in, r.host_in):
+            d_.copy_(h_, non_blocking=True)
+        r.fwd()
+        r.bwd()
+        for h_, d_ in zip(host_out, outs):
+            h_.copy_(d_, non_blocking=True)
+    stop.record(r.stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop), h2d, d2h
+
+
+def cpu_oracle_sample(w: si.Workload, causal: bool, budget_s: float = 12.0, max_rows=None):
+    """Times the float64 oracle (forward + backward) on the first n rows of head 0.
+    With the causal mask those rows see only keys 0..n-1, so this is an exact
+    sub-problem with 4 n^2 d + 10 n^2 d (halved) counted FLOPs.  n doubles from
+    512 until the budget is used."""
+    import oracle
+    Q, K, V, dO = si.make_qkvdo(1, 1, w.N, w.d, seed=w.seed, qk_mult=w.qk_mult)
+    q, k, v, do = (si.to_f64(t)[0, 0] for t in (Q, K, V, dO))
+    n, spent, flops, last = 512, 0.0, 0.0, None
+    limit = min(w.N, max_rows or w.N)
+    while True:
+        t0 = time.perf_counter()
+        oracle.standard_attention_fwd(q[:n], k[:n], v[:n], causal)
+        oracle.standard_attention_bwd(q[:n], k[:n], v[:n], do[:n], causal)
+        dt = time.perf_counter() - t0
+        f = 14.0 * n * n * w.d * (0.5 if causal else 1.0)
+        spent += dt
+        flops += f
+        last = (n, dt, f)
+        if spent >= budget_s or n >= limit or spent + 4.5 * dt > 2.5 * budget_s:
+            break
+        n = min(2 * n, limit)
+    n, dt, f = last
+    return {"value": f / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"float64 NumPy oracle fwd+bwd on query rows 0..{n - 1} of head 0 "
+                      f"({'causal' if causal else 'full'}; an exact sub-problem of {w.name}), "
+                      f"{dt:.2f} s for {f / 1e9:.1f} GFLOP counted"}
+
+
+def run_ours(args):
+    import torch
+
+    import exact_tiled_attention_26_gb300 as fa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    w = si.WORKLOADS[args.workload]
+    causal = True if len(w.causal) == 1 and w.causal[0] else (args.causal if args.causal is not None else w.causal[-1])
+    r = Runner(fa, torch, w, causal, dev)
+    flops_f, flops_b = w.fwd_flops(causal), w.bwd_flops(causal)
+
+    # warm-up (also compiles nothing: the library is prebuilt), then the timed region
+    for _ in range(args.warmup):
+        r.fwd()
+        r.bwd()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        fwd_ms, bwd_ms = time_steps(torch, r, args.steps, 0)
+    st, detail = fa.fa_poll_device_error(r.s)
+    fa.check(st, f"device status word (site {detail:#x})")
+    total_ms = fwd_ms + bwd_ms
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * (flops_f + flops_b) * args.steps / (total_ms / 1e3) / 1e12
+
+    peaks, peak_src = _peaks()
+    sustained = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    bwd_tflops = flops_b * args.steps / (bwd_ms / 1e3) / 1e12
+    fwd_tflops = flops_f * args.steps / (fwd_ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded iid N(0,1) bf16 Q, K, V, dO)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal,
+                   "global_batch": w.B * world, "seq_len": w.N, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+                   "l2": "no flush: inputs (Q, K, V, dO) total "
+                         f"{4 * w.B * w.H * w.N * w.d * 2 / 2**30:.2f} GiB, larger than the 129 MB L2"},
+        "fwd_tflops": round(fwd_tflops, 2), "bwd_tflops": round(bwd_tflops, 2),
+        "frac_of_bf16_peak": round(value / world / sustained, 4),
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "fa_bwd (bwd main kernel, with its workspace memset and dQ convert)",
+            "achieved": round(bwd_tflops, 2), "peak": sustained, "unit": "TFLOP/s",
+            "frac": round(bwd_tflops / sustained, 4), "traffic": None,
+            "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
+            "algorithmic": "10 N^2 d / 2 FLOPs per head (causal) per launch",
+        },
+        "gpu_launches": Runner.LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.quick and rank == 0:
+        # end to end through the C ABI with host buffers
+        steps_e2e = max(2, min(args.steps, 5))
+        ms, h2d, d2h = e2e_steps(torch, r, steps_e2e)
+        line["e2e"] = {"value": round((flops_f + flops_b) * steps_e2e / (ms / 1e3) / 1e12, 2), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(ms / steps_e2e, 3)}
+        line["per_config"] = per_config(fa, torch, dev, peaks)
+        line["cpu_baseline"] = cpu_oracle_sample(w, causal)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def per_config(fa, torch, dev, peaks):
+    """The other full-size shapes, each timed briefly; L2 is flushed before every
+    step (a 256 MiB write) because their inputs are near or below the L2 size."""
+    flush_buf = torch.empty(256 * 2**20, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, causal in (("mid_2x16x4096x128", False), ("mid_2x16x4096x128", True),
+                         ("long_1x32x8192x128", True), ("long_1x32x8192x128_qk4", True),
+                         ("small_4x8x1024x64", True)):
+        w = si.WORKLOADS[name]
+        r = Runner(fa, torch, w, causal, dev)
+        fwd_ms, bwd_ms = time_steps(torch, r, 10, 3, flush=lambda: flush_buf.zero_())
+        ff, fb = w.fwd_flops(causal) * 10, w.bwd_flops(causal) * 10
+        out[f"{name}{'_causal' if causal else ''}"] = {
+            "fwd_tflops": round(ff / fwd_ms / 1e9, 1), "bwd_tflops": round(fb / bwd_ms / 1e9, 1),
+            "fwd_bwd_tflops": round((ff + fb) / (fwd_ms + bwd_ms) / 1e9, 1),
+            "ms_per_step": round((fwd_ms + bwd_ms) / 10, 4)}
+        del r
+    return out
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = si.WORKLOADS[args.workload]
+    causal = True
+    import oracle
+    Q, K, V, dO = si.make_qkvdo(1, 1, w.N, w.d, seed=w.seed, qk_mult=w.qk_mult)
+    q, k, v, do = (si.to_f64(t)[0, 0] for t in (Q, K, V, dO))
+    n = 2048  # rows 0..n-1 of head 0: an exact causal sub-problem of the workload
+    flops = 14.0 * n * n * w.d * 0.5
+
+    def step():
+        oracle.standard_attention_fwd(q[:n], k[:n], v[:n], causal)
+        oracle.standard_attention_bwd(q[:n], k[:n], v[:n], do[:n], causal)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = flops * args.steps / dt / 1e12
+    sample = (f"float64 NumPy oracle fwd+bwd on query rows 0..{n - 1} of head 0 of {w.name} (causal: an exact "
+              f"sub-problem), {flops / 1e9:.2f} GFLOP counted per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded iid N(0,1), bf16-rounded, widened to f64)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--causal", type=int, default=None, help="for workloads that run both mask modes")
+    ap.add_argument("--quick", action="store_true", help="headline timing only (for profiler runs)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and not args.quick:
+        ap.error("at least 3 warm-up steps")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

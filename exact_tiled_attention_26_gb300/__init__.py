@@ -38,7 +38,7 @@ class FAError(RuntimeError):
 def _load():
     if not os.path.exists(lib_path):
         raise ImportError(
-            f"{lib_path} is missing: build it with `python -m exact_tiled_attention_26_gb300.build` "
+            f"{lib_path} is missing: build it with `python exact_tiled_attention_26_gb300/build.py` "
             "(or __graft_entry__.build()); there is no non-CUDA fallback")
     return ctypes.CDLL(lib_path)
 

@@ -1,6 +1,6 @@
 """Build libfa_gb300.so in-tree with nvcc for sm_103a (no cmake, no torch extension).
 
-    python -m exact_tiled_attention_26_gb300.build [--verbose]
+    python exact_tiled_attention_26_gb300/build.py [--verbose] [--ptxas-info]
 
 Each translation unit compiles in parallel into ``_build/``; the objects are
 linked (static CUDA runtime) into ``exact_tiled_attention_26_gb300/libfa_gb300.so``.

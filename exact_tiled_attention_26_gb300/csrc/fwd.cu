@@ -16,8 +16,8 @@
 //               online max/sum in base 2 with the scale folded into one FMA,
 //               P written back as bf16 over its own S columns; epilogue
 // The accumulator is rescaled lazily: only when a row's max grows by more
-// than 2^8 (in base-2 units) is the running max moved and O, l multiplied by
-// 2^(m_old - m_new).  Between moves P <= 2^8, exact in fp32 and bf16 range;
+// than 8 (in base-2 units) is the running max moved and O, l multiplied by
+// 2^(m_old - m_new).  Between moves P <= 2^8, well inside fp32 and bf16 range;
 // O / l is unchanged by the choice of reference max.
 #include "internal.h"
 #include "ptx.cuh"
@@ -185,7 +185,8 @@ __global__ void __launch_bounds__(256, 1)
     const int q = qt * C::BM + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     float m_run = -INFINITY;  // running max of S * scale * log2(e)
-    float l_run = 0.f;
+    float l_run = 0.f;        // running sum of P (for L)
+    float lr_run = 0.f;       // running sum of P as rounded to bf16 for the P V product (for O)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int b = j % C::NSB;
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(256, 1)
           const float alpha = move ? ex2(m_run - m_tile) : 1.f;
           if (move) {
             l_run *= alpha;
+            lr_run *= alpha;
             m_run = m_tile;
           }
           // O holds P_0..P_{j-1} V: wait for the last of those products
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       const float neg_m = -m_run;
-      float lsum0 = 0.f, lsum1 = 0.f;
+      float lsum0 = 0.f, lsum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
       uint32_t p[64];
 #pragma unroll
       for (int k = 0; k < 128; k += 2) {
@@ -244,9 +246,13 @@ __global__ void __launch_bounds__(256, 1)
         const float p1 = ex2(fmaf(s[k + 1], c_log2, neg_m));
         lsum0 += p0;
         lsum1 += p1;
-        p[k >> 1] = pack_bf16x2(p0, p1);
+        const uint32_t pk = pack_bf16x2(p0, p1);
+        p[k >> 1] = pk;
+        rsum0 += __uint_as_float(pk << 16);
+        rsum1 += __uint_as_float(pk & 0xffff0000u);
       }
       l_run += lsum0 + lsum1;
+      lr_run += rsum0 + rsum1;
       tmem_st32(tl + C::TM_S0 + b * 128, p);
       tmem_st32(tl + C::TM_S0 + b * 128 + 32, p + 32);
       tmem_st_wait();
@@ -256,7 +262,9 @@ __global__ void __launch_bounds__(256, 1)
     if (ok) ok = mbar_wait_warp(bar(C::B_OFINAL), 0, guard, SITE_FWD_SOFTMAX);
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      // O is normalised by the sum of the very bf16 weights that entered P V, so
+      // that the weights applied to V sum to one; L uses the unrounded sum.
+      const float inv_l = 1.f / lr_run;
       __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

@@ -74,6 +74,13 @@ def _scores(q_rows: np.ndarray, row_ids: np.ndarray, K: np.ndarray, causal: bool
     return S
 
 
+def _visible(rows: np.ndarray, n_keys: int, causal: bool) -> int:
+    """Keys 0 .. k-1 hold every nonzero weight of these rows.  Under the causal
+    mask, keys after the last row carry weight exp(-inf) = 0 exactly, so leaving
+    them out of the sums changes no value."""
+    return min(n_keys, int(rows.max()) + 1) if causal else n_keys
+
+
 def _logsumexp_rows(S: np.ndarray) -> np.ndarray:
     """Safe logsumexp per row: m + ln(sum exp(S - m)) ([p2] demo1_overflow; [p3] §1.2)."""
     m = S.max(axis=1)
@@ -99,10 +106,11 @@ def standard_attention_fwd(Q, K, V, causal: bool = False, scale=None):
     for h in range(Qh.shape[0]):
         for r0 in range(0, N, ROW_BLOCK):
             rows = np.arange(r0, min(N, r0 + ROW_BLOCK))
-            S = _scores(Qh[h, rows], rows, Kh[h], causal, s)
+            kv = _visible(rows, Kh.shape[1], causal)
+            S = _scores(Qh[h, rows], rows, Kh[h, :kv], causal, s)
             Lr = _logsumexp_rows(S)
             P = np.exp(S - Lr[:, None])  # softmax of each row
-            O[h, rows] = P @ Vh[h]
+            O[h, rows] = P @ Vh[h, :kv]
             L[h, rows] = Lr
     return O.reshape(lead + O.shape[-2:]), L.reshape(lead + (N,))
 
@@ -128,14 +136,15 @@ def standard_attention_bwd(Q, K, V, dO, causal: bool = False, scale=None):
     for h in range(Qh.shape[0]):
         for r0 in range(0, N, ROW_BLOCK):
             rows = np.arange(r0, min(N, r0 + ROW_BLOCK))
-            S = _scores(Qh[h, rows], rows, Kh[h], causal, s)
+            kv = _visible(rows, Kh.shape[1], causal)
+            S = _scores(Qh[h, rows], rows, Kh[h, :kv], causal, s)
             P = np.exp(S - _logsumexp_rows(S)[:, None])
-            dP = dOh[h, rows] @ Vh[h].T
+            dP = dOh[h, rows] @ Vh[h, :kv].T
             Dr = (P * dP).sum(axis=1)
             dS = P * (dP - Dr[:, None])
-            dQ[h, rows] = (dS @ Kh[h]) * s
-            dK[h] += (dS.T @ Qh[h, rows]) * s
-            dV[h] += P.T @ dOh[h, rows]
+            dQ[h, rows] = (dS @ Kh[h, :kv]) * s
+            dK[h, :kv] += (dS.T @ Qh[h, rows]) * s
+            dV[h, :kv] += P.T @ dOh[h, rows]
             D[h, rows] = Dr
     shp = lead + (N, d)
     return (dQ.reshape(shp), dK.reshape(lead + Kh.shape[-2:]),
@@ -167,15 +176,16 @@ def rows_fwd_bwd(Q, K, V, dO, rows, causal: bool = False, scale=None):
     for h in range(BH):
         for b0 in range(0, len(rows), ROW_BLOCK):
             r = rows[b0:b0 + ROW_BLOCK]
-            S = _scores(Q[h, r], r, K[h], causal, s)
+            kv = _visible(r, K.shape[1], causal)
+            S = _scores(Q[h, r], r, K[h, :kv], causal, s)
             Lr = _logsumexp_rows(S)
             P = np.exp(S - Lr[:, None])
-            dP = dO[h, r] @ V[h].T
+            dP = dO[h, r] @ V[h, :kv].T
             Dr = (P * dP).sum(axis=1)
-            O[h, b0:b0 + len(r)] = P @ V[h]
+            O[h, b0:b0 + len(r)] = P @ V[h, :kv]
             L[h, b0:b0 + len(r)] = Lr
             D[h, b0:b0 + len(r)] = Dr
-            dQ[h, b0:b0 + len(r)] = ((P * (dP - Dr[:, None])) @ K[h]) * s
+            dQ[h, b0:b0 + len(r)] = ((P * (dP - Dr[:, None])) @ K[h, :kv]) * s
     return O, L, dQ, D
 
 
@@ -194,9 +204,10 @@ def key_rows_bwd(Q, K, V, dO, L, D, keys, causal: bool = False, scale=None):
     BH = Q.shape[0]
     dK = np.zeros((BH, len(keys), d))
     dV = np.zeros((BH, len(keys), V.shape[-1]))
+    first = int(keys.min()) if causal else 0  # rows before the first key see none of them
     for h in range(BH):
         Kk, Vk = K[h, keys], V[h, keys]
-        for r0 in range(0, N, ROW_BLOCK):
+        for r0 in range(first - first % ROW_BLOCK, N, ROW_BLOCK):
             rows = np.arange(r0, min(N, r0 + ROW_BLOCK))
             S = (Q[h, rows] @ Kk.T) * s
             if causal:

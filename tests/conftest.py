@@ -32,7 +32,7 @@ def fa_lib():
     """The ctypes binding, building libfa_gb300.so first if it is missing."""
     lib_path = os.path.join(ROOT, "exact_tiled_attention_26_gb300", "libfa_gb300.so")
     if not os.path.exists(lib_path):
-        from exact_tiled_attention_26_gb300.build import build
-        build()
+        import __graft_entry__
+        __graft_entry__.build()
     import exact_tiled_attention_26_gb300 as fa
     return fa

@@ -5,6 +5,13 @@ Tolerances (element-wise against the oracle run on the bf16-rounded inputs):
   O:  max |err| <= 1e-2 and ||err||_F / ||ref||_F <= 5e-3
   L:  max |err| <= 2e-3
   dQ, dK, dV: ||err||_F / ||ref||_F <= 1e-2
+
+O is returned in bf16, whose own rounding reaches half a bf16 unit in the last
+place of |O| (0.0078 for |O| in [2, 4), 0.0156 for |O| in [4, 8)).  The max-abs
+bound on O therefore applies to the error beyond that quantum:
+|got - ref| - ulp_bf16(ref)/2 <= 1e-2.  A gradient whose exact value is zero
+(e.g. dQ and dK with a single key) is checked by its RMS (<= 1e-4) instead of
+the relative norm.
 """
 from __future__ import annotations
 
@@ -20,6 +27,17 @@ TOL_O_ABS, TOL_O_REL, TOL_L_ABS, TOL_G_REL = 1e-2, 5e-3, 2e-3, 1e-2
 
 def rel_frob(got, ref):
     return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def half_ulp_bf16(x):
+    """Half the spacing of bf16 numbers at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return np.ldexp(1.0, np.floor(np.log2(ax)).astype(np.int64) - 8)
+
+
+def o_excess(got, ref):
+    """max(|got - ref| - half a bf16 ulp of ref): the O error beyond output rounding."""
+    return float((np.abs(got - ref) - half_ulp_bf16(ref)).max())
 
 
 def stream():
@@ -77,10 +95,11 @@ def assert_close(got: dict, ref: dict, label=""):
     msgs = []
     errs = {}
     if "O" in ref:
-        ea, er = float(np.abs(got["O"] - ref["O"]).max()), rel_frob(got["O"], ref["O"])
-        errs["O"] = (ea, er)
-        if not (ea <= TOL_O_ABS and er <= TOL_O_REL):
-            msgs.append(f"O max-abs {ea:.3e} rel {er:.3e}")
+        ea, ex, er = float(np.abs(got["O"] - ref["O"]).max()), o_excess(got["O"], ref["O"]), rel_frob(got["O"], ref["O"])
+        errs["O"] = (ea, ex, er)
+        if not (ex <= TOL_O_ABS and er <= TOL_O_REL):
+            i = np.unravel_index(np.argmax(np.abs(got["O"] - ref["O"])), ref["O"].shape)
+            msgs.append(f"O max-abs {ea:.3e} (beyond output rounding {ex:.3e}, at ref {ref['O'][i]:.4f}) rel {er:.3e}")
     if "L" in ref:
         ea = float(np.abs(got["L"] - ref["L"]).max())
         errs["L"] = ea
@@ -88,6 +107,12 @@ def assert_close(got: dict, ref: dict, label=""):
             msgs.append(f"L max-abs {ea:.3e}")
     for n in ("dQ", "dK", "dV"):
         if n in ref:
+            if np.linalg.norm(ref[n]) <= 1e-9:
+                rms = float(np.sqrt(np.mean(got[n] ** 2)))
+                errs[n] = rms
+                if not rms <= 1e-4:
+                    msgs.append(f"{n} (exactly zero) rms {rms:.3e}")
+                continue
             er = rel_frob(got[n], ref[n])
             errs[n] = er
             if not er <= TOL_G_REL:
