@@ -18,6 +18,7 @@ import os
 __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_WORKSPACE",
     "FAError", "lib", "lib_path", "fa_fwd", "fa_bwd_preprocess", "fa_bwd_workspace_size", "fa_bwd",
+    "fa_bwd_noalloc", "FA_NOALLOC_MAX_WORKSPACE_BYTES",
     "fa_status_string", "fa_get_tile_config", "fa_tile_pairs", "fa_debug_set_tile_counter",
     "fa_poll_device_error", "fa_debug_timeout_probe", "fa_selftest_umma", "fa_version",
     "attention_forward", "attention_backward", "check",
@@ -51,6 +52,7 @@ _sig = {
     "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
+    "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_get_tile_config": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fa_tile_pairs": (ctypes.c_longlong, [_i, _i, _i, _i]),
@@ -82,6 +84,15 @@ def fa_bwd_workspace_size(B, H, N, d, causal):
 def fa_bwd(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, N, d, causal, scale, workspace, workspace_bytes, stream):
     return lib.fa_bwd(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, N, d, int(bool(causal)), scale, workspace,
                       workspace_bytes, stream)
+
+
+FA_NOALLOC_MAX_WORKSPACE_BYTES = 16 << 20
+
+
+def fa_bwd_noalloc(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, N, d, causal, scale, stream):
+    """fa_bwd without a caller-provided workspace (see include/fa.h): for callers
+    that cannot allocate device memory; limited to B*H*N*d*4 <= 16 MiB."""
+    return lib.fa_bwd_noalloc(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, N, d, int(bool(causal)), scale, stream)
 
 
 def fa_status_string(status):

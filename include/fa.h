@@ -102,6 +102,36 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  int B, int H, int N, int d, int causal, float scale,
                  void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
+/*
+ * Largest workspace fa_bwd_noalloc can provide: B*H*N*d*4 bytes must not exceed
+ * it (16 MiB, e.g. B*H*N = 32768 rows at d = 128).
+ */
+#define FA_NOALLOC_MAX_WORKSPACE_BYTES (16u << 20)
+
+/*
+ * fa_bwd for callers that cannot allocate device memory when they run the
+ * backward: for example, code working inside device memory that a host
+ * framework or serving runtime has reserved up front (no allocations outside
+ * its pool), or code that must not call cudaMalloc/cudaFree because those can
+ * synchronise the device.  The pages have no counterpart: this entry point
+ * exists only for such callers.
+ *
+ * Same arguments, results and errors as fa_bwd, without the workspace: the fp32
+ * dQ accumulator is a fixed array inside the library (one per device that
+ * loads it, held until the process exits), so the call allocates nothing.
+ *   - Returns FA_ERR_WORKSPACE, without enqueuing anything, when
+ *     B*H*N*d*4 > FA_NOALLOC_MAX_WORKSPACE_BYTES.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the array, which keeps the last call's
+ *     contents; each call zeroes it on `stream` first.  Calls on the same device
+ *     whose work overlaps on the GPU race on it: serialise them.
+ */
+fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                         const float* L, const float* D, void* dQ, void* dK, void* dV,
+                         int B, int H, int N, int d, int causal, float scale, fa_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(fa_status s);
 
