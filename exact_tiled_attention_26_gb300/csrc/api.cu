@@ -223,7 +223,8 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
               stream, status, g_tile_counter};
   st = launch_bwd(a);
   if (st != FA_OK) return st;
-  return launch_dq_convert(static_cast<const float*>(workspace), dQ, static_cast<long long>(B) * H * N * d, stream);
+  return launch_dq_convert(static_cast<const float*>(workspace), dQ, static_cast<long long>(B) * H * N * d, scale,
+                           stream);
 }
 
 fa_status fa_poll_device_error(fa_stream_t stream, int* detail) {

@@ -2,7 +2,7 @@
 //
 //  * preprocess: D_i = sum_k dO_ik O_ik ("CS336 Assignment 2 notes" §1.4,
 //    Eq 17, D = rowsum(O * dO)); one pass over O and dO.
-//  * dq_convert: rounds the fp32 dQ accumulator to bf16.
+//  * dq_convert: scales the fp32 dQ accumulator and rounds it to bf16.
 //  * timeout probe: one time-limited wait that can never complete.
 //  * UMMA self-test: one 128 x N x K tile product through the operand paths
 //    (K-major / M,N-major shared memory, tensor-memory A) of the attention kernels.
@@ -70,17 +70,20 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
   }
 }
 
+// dQ = bf16(scale * sum over key tiles of dS K): the softmax scale of Eq 18 is
+// applied here, once per element, instead of to every dS element.
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ src,
-                                                         __nv_bfloat16* __restrict__ dst, long long n8) {
+                                                         __nv_bfloat16* __restrict__ dst, long long n8,
+                                                         float scale) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
     const uint4 lo = ld_stream_v4(src + 8 * i);
     const uint4 hi = ld_stream_v4(src + 8 * i + 4);
     uint4 out;
-    out.x = pack_bf16x2(__uint_as_float(lo.x), __uint_as_float(lo.y));
-    out.y = pack_bf16x2(__uint_as_float(lo.z), __uint_as_float(lo.w));
-    out.z = pack_bf16x2(__uint_as_float(hi.x), __uint_as_float(hi.y));
-    out.w = pack_bf16x2(__uint_as_float(hi.z), __uint_as_float(hi.w));
+    out.x = pack_bf16x2(__uint_as_float(lo.x) * scale, __uint_as_float(lo.y) * scale);
+    out.y = pack_bf16x2(__uint_as_float(lo.z) * scale, __uint_as_float(lo.w) * scale);
+    out.z = pack_bf16x2(__uint_as_float(hi.x) * scale, __uint_as_float(hi.y) * scale);
+    out.w = pack_bf16x2(__uint_as_float(hi.z) * scale, __uint_as_float(hi.w) * scale);
     *reinterpret_cast<uint4*>(dst + 8 * i) = out;
   }
 }
@@ -253,12 +256,13 @@ fa_status launch_preprocess(const void* O, const void* dO, float* D, long long r
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-fa_status launch_dq_convert(const float* dQacc, void* dQ, long long n, cudaStream_t s) {
+fa_status launch_dq_convert(const float* dQacc, void* dQ, long long n, float scale, cudaStream_t s) {
   const long long n8 = n / 8;
   long long blocks = (n8 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(dQacc, static_cast<__nv_bfloat16*>(dQ), n8);
+  dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(dQacc, static_cast<__nv_bfloat16*>(dQ), n8,
+                                                                   scale);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -1,4 +1,5 @@
-// Backward pass of exact tiled attention on sm_103a (main kernel).
+// Backward pass of exact tiled attention on sm_103a: main kernel for head sizes
+// 32 and 64 (head size 128 has its own pipelined kernel in bwd128.cu).
 //
 // "CS336 Assignment 2 notes" §1.4, Equations 13-19, with the key/value tiles
 // in the outer loop (kernel 1 of the notes' two-kernel scheme).  One CTA owns
@@ -10,7 +11,8 @@
 //   P^T  = exp(S^T - L_i)                   (Eq 14; L from the forward)
 //   dV_j += P^T dO_i                        (Eq 15; P^T read from tensor memory)
 //   dP^T = V_j dO_i^T                       (Eq 16)
-//   dS^T = P^T * (dP^T - D_i) * scale       (Eq 17; D from the preprocess)
+//   dS^T = P^T * (dP^T - D_i)               (Eq 17; D from the preprocess; the scale
+//                                            of Eq 18-19 is applied to dK and dQ at the end)
 //   dK_j += dS^T Q_i                        (Eq 19; dS from shared memory)
 //   dQ_i += dS K_j                          (Eq 18) formed per tile in tensor
 //           memory and added into an fp32 [B,H,N,d] workspace with one bulk
@@ -252,7 +254,7 @@ __global__ void __launch_bounds__(256, 1)
             const int ql = 32 * c + x + y;  // query within the tile
             float p = ex2(fmaf(__uint_as_float(rs[x + y]), c_log2, -Ls[ql]));
             if (masked && ((CAUSAL && key > q0 + ql) || key >= N)) p = 0.f;
-            const float ds = p * (__uint_as_float(rp[x + y]) - Ds[ql]) * scale;
+            const float ds = p * (__uint_as_float(rp[x + y]) - Ds[ql]);
             pv[y] = p;
             *reinterpret_cast<__nv_bfloat16*>(dSs + swz128_offset<C::BM>(ql, kr)) = __float2bfloat16_rn(ds);
           }
@@ -319,14 +321,15 @@ __global__ void __launch_bounds__(256, 1)
           uint32_t r[32];
           tmem_ld32(tl + col + 32 * c, r);
           tmem_ld_wait<32>(r);
+          const float f = t == 0 ? scale : 1.f;  // Eq 19's scale, applied once to dK
           if (key < N) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+              d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * f, __uint_as_float(r[8 * i + 1]) * f),
+                                 pack_bf16x2(__uint_as_float(r[8 * i + 2]) * f, __uint_as_float(r[8 * i + 3]) * f),
+                                 pack_bf16x2(__uint_as_float(r[8 * i + 4]) * f, __uint_as_float(r[8 * i + 5]) * f),
+                                 pack_bf16x2(__uint_as_float(r[8 * i + 6]) * f, __uint_as_float(r[8 * i + 7]) * f));
           }
         }
       }
@@ -369,7 +372,7 @@ fa_status launch_bwd(const BwdLaunch& a) {
   switch (a.d) {
     case 32: return a.causal ? launch_bwd_t<32, true>(a) : launch_bwd_t<32, false>(a);
     case 64: return a.causal ? launch_bwd_t<64, true>(a) : launch_bwd_t<64, false>(a);
-    case 128: return a.causal ? launch_bwd_t<128, true>(a) : launch_bwd_t<128, false>(a);
+    case 128: return launch_bwd_d128(a);  // software-pipelined kernel of bwd128.cu
     default: return FA_ERR_UNSUPPORTED;
   }
 }

@@ -49,9 +49,10 @@ struct BwdLaunch {
   unsigned long long* counter;
 };
 fa_status launch_bwd(const BwdLaunch& a);
+fa_status launch_bwd_d128(const BwdLaunch& a);
 
 fa_status launch_preprocess(const void* O, const void* dO, float* D, long long rows, int d, cudaStream_t s);
-fa_status launch_dq_convert(const float* dQacc, void* dQ, long long n, cudaStream_t s);
+fa_status launch_dq_convert(const float* dQacc, void* dQ, long long n, float scale, cudaStream_t s);
 fa_status launch_timeout_probe(int limit_us, cudaStream_t s, int* status);
 fa_status launch_selftest(int mode, const void* A, const void* B, float* C, int K, int N, cudaStream_t s,
                           int* status);
