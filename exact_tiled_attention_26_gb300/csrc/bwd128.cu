@@ -1,27 +1,34 @@
-// Backward pass, head size 128: the software-pipelined main kernel.
+// Backward pass, head size 128: the main kernel.
 //
 // Same mathematics as bwd.cu ("CS336 Assignment 2 notes" §1.4, Equations 13-19,
-// key/value tiles outer): one CTA owns 128 keys of one (batch, head), K_j and V_j
-// stay in shared memory, and the CTA walks the visible 64-row query tiles i.
-// With keys on the 128 tensor-memory lanes:
+// key/value tiles outer): one CTA owns 128 keys of one (batch, head); K_j and
+// V_j stay in shared memory while the CTA walks the visible 128-row query tiles
+// i.  With keys on the 128 tensor-memory lanes, per step:
 //
-//   S^T(i)  = K Q_i^T,  dP^T(i) = V dO_i^T                          (UMMA)
-//   P^T     = 2^(S^T c - L log2 e),  dS^T = P^T (dP^T - D)           (8 warps)
-//   dV += P^T dO_i (P^T from tensor memory),  dK += dS^T Q_i,
-//   dQ_i^T  = K^T dS^T  (into the dP^T columns of the same step)     (UMMA)
-//   dQ_i   += dQ_i^T-tile, added into the fp32 workspace with one bulk reduce
-//             per tile (performed in L2).  The softmax scale of Eq 18-19 is
-//             applied to dK here at the end and to dQ by the convert pass.
+//   S^T  = K Q_i^T                       (UMMA, M=N=128)          Eq 13
+//   P^T  = 2^(S^T c - L log2 e) -> bf16, kept in tensor memory     Eq 14
+//   dP^T = V dO_i^T                      (UMMA)                   Eq 16
+//   dV  += P^T dO_i                      (UMMA, A = P^T in TMEM)   Eq 15
+//   dS^T = P^T (dP^T - D) -> bf16, in tensor memory and in shared memory (Eq 17)
+//   dK  += dS^T Q_i                      (UMMA, A = dS^T in TMEM)  Eq 19
+//   dQ_i^T = K^T dS^T                    (UMMA, over the dP^T columns)
+//   dQ_i += dQ_i^T, added from registers into the fp32 workspace with
+//           coalesced reductions in L2                             Eq 18
+// The softmax scale of Eq 18-19 is applied to dK at the end and to dQ by the
+// convert pass.
 //
-// The UMMA issuer runs one step ahead: S^T(i+1) and dP^T(i+1) go to the other of
-// two tensor-memory buffers while the element-wise warps work on step i, so the
-// tensor pipe has work while P and dS are formed.  Tensor memory (512 columns):
-// dK 128 | dV 128 | S^T x2 (64 each) | dP^T / dQ^T x2 (64 each).
+// Every UMMA is M = 128, N = 128 (narrower UMMAs do not reach the tensor pipe's
+// rate).  Tensor memory (512 columns): dK 128 | dV 128 | S^T region 128 | dP^T
+// region 128.  In the S^T region, query half h (64 queries) keeps its bf16 P^T in
+// columns 64h .. 64h+31 and its bf16 dS^T in 64h+32 .. 64h+63, overwriting only
+// its own S^T.  The UMMA issue order S, dP, dV, dK, dQ^T, S(next), ... keeps the
+// tensor pipe busy while the element-wise warps form P (during dP), dS (during
+// dV) and hand dQ to L2 (during the next S).
 //
-// Warps: 0 TMA producer (all lanes also stage L*log2 e and D of each query tile
-// in shared memory, two tiles ahead), 1 UMMA issuer (one thread), 2 dQ reducer
-// (one thread issues the bulk adds), 4..11 element-wise (warp w: tensor-memory
-// lane quarter w % 4, query half (w - 4) / 4; one key row per thread).
+// Warps: 0 TMA producer (its 32 lanes also stage L*log2 e and D of each query
+// tile in shared memory, two tiles ahead), 1 UMMA issuer (one thread), 4..11
+// element-wise (warp w: tensor-memory lane quarter w % 4, query half (w - 4) / 4;
+// one key row per thread, which is also the d index of dQ^T).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -31,34 +38,31 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct B128 {
-  static constexpr int D = 128, BN = 128, BM = 64;
+  static constexpr int D = 128, BN = 128, BM = 128;
   static constexpr int NTHREADS = 384;
-  static constexpr int KV_BYTES = BN * D * 2;   // 32 KB
-  static constexpr int QT_BYTES = BM * D * 2;   // 16 KB
-  static constexpr int DS_BYTES = BN * BM * 2;  // 16 KB: dS^T [128 keys][64 queries], 128-byte rows
-  static constexpr int DQ_BYTES = BM * D * 4;   // 32 KB: fp32 dQ tile [64][128]
-  static constexpr int LD_BYTES = 2 * BM * 4;   // L*log2 e [64], D [64]
-  static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;        // 2 stages
-  static constexpr int OFF_DO = OFF_Q + 2 * QT_BYTES;   // 2 stages
-  static constexpr int OFF_DS = OFF_DO + 2 * QT_BYTES;  // 2 buffers
-  static constexpr int OFF_DQ = OFF_DS + 2 * DS_BYTES;
-  static constexpr int OFF_LD = OFF_DQ + DQ_BYTES;      // 2 stages
-  static constexpr int OFF_BAR = OFF_LD + 2 * LD_BYTES;
+  static constexpr int NCOMP = 256;             // element-wise threads
+  static constexpr int TILE = 128 * 128 * 2;    // one 128 x 128 bf16 tile (two 64-column chunks)
+  // small region at the start of dynamic shared memory
   enum : int {
-    B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 7, B_PREADY = 9, B_DVDONE = 11,
-    B_DQFULL = 13, B_DQCONS = 15, B_DQSFULL = 17, B_DQSEMPTY = 18, B_FINAL = 19, NBAR = 20
+    B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6, B_PREADY = 7, B_DSREADY = 8, B_DKDONE = 9,
+    B_DQFULL = 10, B_DQCONS = 11, B_FINAL = 12, NBAR = 13
   };
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_BAR = 0;
+  static constexpr int OFF_MISC = NBAR * 8;     // tensor-memory base, abort flag
+  static constexpr int OFF_LD = 256;            // 2 stages x (L*log2 e [128], D [128])
+  static constexpr int LD_BYTES = 2 * BM * 4;
+  static constexpr int SMALL = OFF_LD + 2 * LD_BYTES;
+  // 1 KiB-aligned tiles after it
+  static constexpr int T_K = 0, T_V = TILE, T_Q = 2 * TILE, T_DO = 3 * TILE;  // Q, dO: stage s adds s * 2 * TILE
+  static constexpr int T_DS = 6 * TILE;         // dS^T [128 keys][128 queries]
+  static constexpr int TILES = 7 * TILE;        // 224 KiB
+  static constexpr int SMEM = 232448;           // the per-block maximum
   static constexpr int TM_DK = 0, TM_DV = 128, TM_S = 256, TM_DP = 384, TM_COLS = 512;
-  static constexpr int NCOMP = 256;  // element-wise threads
-  static_assert(OFF_DS % 1024 == 0 && OFF_Q % 1024 == 0 && OFF_DO % 1024 == 0, "swizzled tiles need 1 KiB alignment");
-  static_assert(SMEM <= 232448, "shared memory budget");
+  // with a 1 KiB-aligned base the tiles start at 3 KiB and end exactly at the limit
+  static_assert(SMALL <= 3072 && 3072 + TILES <= SMEM, "shared memory budget");
 };
 
-enum : int { SITE_PRODUCER = 0x211, SITE_MMA = 0x212, SITE_COMPUTE = 0x213, SITE_REDUCER = 0x214 };
+enum : int { SITE_PRODUCER = 0x211, SITE_MMA = 0x212, SITE_COMPUTE = 0x213, SITE_LAYOUT = 0x215 };
 
 template <bool CAUSAL>
 __global__ void __launch_bounds__(B128::NTHREADS, 1)
@@ -68,36 +72,41 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
                     __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int N, float c_log2, float scale,
                     int* status, unsigned long long* tile_counter) {
   using C = B128;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  const uint32_t sb = smem_u32(smem);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* tiles = align1024(smem_raw + C::SMALL);
+  if (tiles + C::TILES > smem_raw + C::SMEM) {
+    // the dynamic shared memory base is too badly aligned for this layout: report, do nothing
+    if (threadIdx.x == 0) atomicCAS(status, 0, SITE_LAYOUT);
+    return;
+  }
+  const uint32_t sb = smem_u32(smem_raw);
+  const uint32_t tb = smem_u32(tiles);
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + C::OFF_MISC + 4);
   const Guard guard{status, abort_flag};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kt = blockIdx.x;  // key tile: with the causal mask the longest loops come first
   const int bh = blockIdx.y;
   const int Tq = (N + C::BM - 1) / C::BM;
-  const int i0 = CAUSAL ? (kt * C::BN) / C::BM : 0;  // first query tile with a visible entry
+  const int i0 = CAUSAL ? kt : 0;  // first query tile with a visible entry (BM == BN)
   const int n_it = Tq - i0;
   const size_t row0 = static_cast<size_t>(bh) * N;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_KV), 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(C::B_QFULL + b), 1 + 32);  // TMA bytes + the producer's 32 lanes (L, D)
-      mbar_init(bar(C::B_QEMPTY + b), 1);
-      mbar_init(bar(C::B_SFULL + b), 1);
-      mbar_init(bar(C::B_DPFULL + b), 1);
-      mbar_init(bar(C::B_PREADY + b), C::NCOMP);
-      mbar_init(bar(C::B_DVDONE + b), 1);
-      mbar_init(bar(C::B_DQFULL + b), 1);
-      mbar_init(bar(C::B_DQCONS + b), C::NCOMP);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_QFULL + s), 1 + 32);  // TMA bytes + the producer's 32 lanes (L, D)
+      mbar_init(bar(C::B_QEMPTY + s), 1);
     }
-    mbar_init(bar(C::B_DQSFULL), C::NCOMP);
-    mbar_init(bar(C::B_DQSEMPTY), 1);
+    mbar_init(bar(C::B_SFULL), 1);
+    mbar_init(bar(C::B_DPFULL), 1);
+    mbar_init(bar(C::B_PREADY), C::NCOMP);
+    mbar_init(bar(C::B_DSREADY), C::NCOMP);
+    mbar_init(bar(C::B_DKDONE), 1);
+    mbar_init(bar(C::B_DQFULL), 1);
+    mbar_init(bar(C::B_DQCONS), C::NCOMP);
     mbar_init(bar(C::B_FINAL), 1);
     *abort_flag = (*reinterpret_cast<volatile int*>(status) != 0);
     fence_mbar_init();
@@ -120,32 +129,38 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
   if (warp == 0 && !skip) {
     // ---------------------------------------------------------------- producer (whole warp)
     if (lane == 0) {
-      mbar_expect_tx(bar(C::B_KV), 2 * C::KV_BYTES);
+      mbar_expect_tx(bar(C::B_KV), 2 * C::TILE);
       for (int c = 0; c < 2; ++c) {
-        tma_load_3d(sb + C::OFF_K + c * C::BN * 128, &tmK, bar(C::B_KV), c * 64, kt * C::BN, bh);
-        tma_load_3d(sb + C::OFF_V + c * C::BN * 128, &tmV, bar(C::B_KV), c * 64, kt * C::BN, bh);
+        tma_load_3d(tb + C::T_K + c * 128 * 128, &tmK, bar(C::B_KV), c * 64, kt * C::BN, bh);
+        tma_load_3d(tb + C::T_V + c * 128 * 128, &tmV, bar(C::B_KV), c * 64, kt * C::BN, bh);
       }
     }
     int last = -1;
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
-      if (!mbar_wait_warp(bar(C::B_QEMPTY + s), ((it >> 1) & 1) ^ 1, guard, SITE_PRODUCER)) break;
       const int q0 = (i0 + it) * C::BM;
+      // L (times log2 e) and D of this query tile, read before waiting for the stage;
+      // rows past N get L = +inf so that their P is exactly 0
+      float lv[4], dv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + lane + 32 * u;
+        lv[u] = q < N ? Lg[row0 + q] * kLog2e : INFINITY;
+        dv[u] = q < N ? Dg[row0 + q] : 0.f;
+      }
+      if (!mbar_wait_warp(bar(C::B_QEMPTY + s), ((it >> 1) & 1) ^ 1, guard, SITE_PRODUCER)) break;
       if (lane == 0) {
-        mbar_expect_tx(bar(C::B_QFULL + s), 2 * C::QT_BYTES);
+        mbar_expect_tx(bar(C::B_QFULL + s), 2 * C::TILE);
         for (int c = 0; c < 2; ++c) {
-          tma_load_3d(sb + C::OFF_Q + s * C::QT_BYTES + c * C::BM * 128, &tmQ, bar(C::B_QFULL + s), c * 64, q0, bh);
-          tma_load_3d(sb + C::OFF_DO + s * C::QT_BYTES + c * C::BM * 128, &tmdO, bar(C::B_QFULL + s), c * 64, q0,
-                      bh);
+          tma_load_3d(tb + C::T_Q + s * 2 * C::TILE + c * 128 * 128, &tmQ, bar(C::B_QFULL + s), c * 64, q0, bh);
+          tma_load_3d(tb + C::T_DO + s * 2 * C::TILE + c * 128 * 128, &tmdO, bar(C::B_QFULL + s), c * 64, q0, bh);
         }
       }
-      // L (times log2 e) and D of this query tile; rows past N get L = +inf so that P = 0
-      float* Ls = reinterpret_cast<float*>(smem + C::OFF_LD + s * C::LD_BYTES);
+      float* Ls = reinterpret_cast<float*>(smem_raw + C::OFF_LD + s * C::LD_BYTES);
 #pragma unroll
-      for (int r = lane; r < C::BM; r += 32) {
-        const int q = q0 + r;
-        Ls[r] = q < N ? Lg[row0 + q] * kLog2e : INFINITY;
-        Ls[C::BM + r] = q < N ? Dg[row0 + q] : 0.f;
+      for (int u = 0; u < 4; ++u) {
+        Ls[lane + 32 * u] = lv[u];
+        Ls[C::BM + lane + 32 * u] = dv[u];
       }
       mbar_arrive(bar(C::B_QFULL + s));
       last = it;
@@ -157,163 +172,158 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     }
   } else if (warp == 1 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- UMMA issuer
-    constexpr uint32_t idS = idesc_bf16(128, C::BM, false, false);  // K|V (K-major) x Q|dO (K-major)
-    constexpr uint32_t idDV = idesc_bf16(128, C::D, false, true);   // P^T (tensor memory) x dO (N-major)
-    constexpr uint32_t idDK = idesc_bf16(128, C::D, false, true);   // dS^T (K-major) x Q (N-major)
-    constexpr uint32_t idDQ = idesc_bf16(128, C::BM, true, true);   // K^T (M-major) x dS^T (N-major)
-    const uint32_t kb = sb + C::OFF_K, vb = sb + C::OFF_V;
-    auto issue_S = [&](int it) {
-      const int b = it & 1;
-      const uint32_t qb = sb + C::OFF_Q + b * C::QT_BYTES;
-#pragma unroll
-      for (int ks = 0; ks < C::D / 16; ++ks)
-        mma_ss(tmem + C::TM_S + 64 * b, sdesc_kmajor<128, C::BN>(kb, ks), sdesc_kmajor<128, C::BM>(qb, ks), idS,
-               ks > 0);
-      mma_commit(bar(C::B_SFULL + b));
-    };
-    auto issue_dP = [&](int it) {
-      const int b = it & 1;
-      const uint32_t db = sb + C::OFF_DO + b * C::QT_BYTES;
-#pragma unroll
-      for (int ks = 0; ks < C::D / 16; ++ks)
-        mma_ss(tmem + C::TM_DP + 64 * b, sdesc_kmajor<128, C::BN>(vb, ks), sdesc_kmajor<128, C::BM>(db, ks), idS,
-               ks > 0);
-      mma_commit(bar(C::B_DPFULL + b));
-    };
+    constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T: K-major x K-major
+    constexpr uint32_t idTN = idesc_bf16(128, 128, false, true);   // dV, dK: A in TMEM x N-major B
+    constexpr uint32_t idMN = idesc_bf16(128, 128, true, true);    // dQ^T: K^T (M-major) x dS^T (N-major)
+    const uint32_t kb = tb + C::T_K, vb = tb + C::T_V, dsb = tb + C::T_DS;
     bool ok = mbar_wait(bar(C::B_KV), 0, guard, SITE_MMA);
-    if (ok && n_it > 0) ok = mbar_wait(bar(C::B_QFULL), 0, guard, SITE_MMA);
-    if (ok && n_it > 0) {
-      tc_fence_after();
-      issue_S(0);
-      issue_dP(0);
-    }
     for (int it = 0; ok && it < n_it; ++it) {
-      const int b = it & 1, nb = b ^ 1;
-      if (it + 1 < n_it) {
-        if (!(ok = mbar_wait(bar(C::B_QFULL + nb), ((it + 1) >> 1) & 1, guard, SITE_MMA))) break;
-        // S^T(it+1) overwrites the columns that held P^T(it-1): dV(it-1) must have read them
-        if (it >= 1 && !(ok = mbar_wait(bar(C::B_DVDONE + nb), ((it - 1) >> 1) & 1, guard, SITE_MMA))) break;
-        tc_fence_after();
-        issue_S(it + 1);
-        // dP^T(it+1) overwrites dQ^T(it-1): the element-wise warps must have read it
-        if (it >= 1 && !(ok = mbar_wait(bar(C::B_DQCONS + nb), ((it - 1) >> 1) & 1, guard, SITE_MMA))) break;
-        tc_fence_after();
-        issue_dP(it + 1);
-      }
-      if (!(ok = mbar_wait(bar(C::B_PREADY + b), (it >> 1) & 1, guard, SITE_MMA))) break;
+      const int s = it & 1;
+      const uint32_t qb = tb + C::T_Q + s * 2 * C::TILE, db = tb + C::T_DO + s * 2 * C::TILE;
+      if (!(ok = mbar_wait(bar(C::B_QFULL + s), (it >> 1) & 1, guard, SITE_MMA))) break;
+      // the S^T region held P^T and dS^T of the previous step until dV and dK read them
+      if (it > 0 && !(ok = mbar_wait(bar(C::B_DKDONE), (it - 1) & 1, guard, SITE_MMA))) break;
       tc_fence_after();
-      const uint32_t qb = sb + C::OFF_Q + b * C::QT_BYTES;
-      const uint32_t db = sb + C::OFF_DO + b * C::QT_BYTES;
-      const uint32_t dsb = sb + C::OFF_DS + b * C::DS_BYTES;
-      const uint32_t aP = tmem + C::TM_S + 64 * b;
-      // dV += P^T dO_i: P^T of queries 0..31 sits in columns 0..15, of 32..63 in 32..47
 #pragma unroll
-      for (int ks = 0; ks < C::BM / 16; ++ks)
-        mma_ts(tmem + C::TM_DV, aP + (ks >> 1) * 32 + (ks & 1) * 8, sdesc_mnmajor<128, C::BM>(db, ks), idDV,
-               (it > 0 || ks > 0));
-      mma_commit(bar(C::B_DVDONE + b));
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tmem + C::TM_S, sdesc_kmajor<128, 128>(kb, ks), sdesc_kmajor<128, 128>(qb, ks), idKK, ks > 0);
+      mma_commit(bar(C::B_SFULL));
+      // the dP^T region held dQ^T of the previous step until it was read
+      if (it > 0 && !(ok = mbar_wait(bar(C::B_DQCONS), (it - 1) & 1, guard, SITE_MMA))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tmem + C::TM_DP, sdesc_kmajor<128, 128>(vb, ks), sdesc_kmajor<128, 128>(db, ks), idKK, ks > 0);
+      mma_commit(bar(C::B_DPFULL));
+      // dV += P^T dO_i  (P^T of query block ks: half ks/4, columns (ks%4)*8 of it)
+      if (!(ok = mbar_wait(bar(C::B_PREADY), it & 1, guard, SITE_MMA))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ts(tmem + C::TM_DV, tmem + C::TM_S + 64 * (ks >> 2) + (ks & 3) * 8, sdesc_mnmajor<128, 128>(db, ks),
+               idTN, (it > 0 || ks > 0));
       // dK += dS^T Q_i
+      if (!(ok = mbar_wait(bar(C::B_DSREADY), it & 1, guard, SITE_MMA))) break;
+      tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < C::BM / 16; ++ks)
-        mma_ss(tmem + C::TM_DK, sdesc_kmajor<128, C::BN>(dsb, ks), sdesc_mnmajor<128, C::BM>(qb, ks), idDK,
-               (it > 0 || ks > 0));
-      // dQ_i^T = K^T dS^T, into the dP^T columns of this step
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ts(tmem + C::TM_DK, tmem + C::TM_S + 64 * (ks >> 2) + 32 + (ks & 3) * 8,
+               sdesc_mnmajor<128, 128>(qb, ks), idTN, (it > 0 || ks > 0));
+      mma_commit(bar(C::B_DKDONE));
+      mma_commit(bar(C::B_QEMPTY + s));  // Q_i, dO_i have no later reader
+      // dQ_i^T = K^T dS^T over the dP^T columns (the element-wise warps have read dP^T)
 #pragma unroll
-      for (int ks = 0; ks < C::BN / 16; ++ks)
-        mma_ss(tmem + C::TM_DP + 64 * b, sdesc_mnmajor<128, C::BN>(kb, ks), sdesc_mnmajor<128, C::BN>(dsb, ks), idDQ,
-               ks > 0);
-      mma_commit(bar(C::B_DQFULL + b));
-      mma_commit(bar(C::B_QEMPTY + b));
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tmem + C::TM_DP, sdesc_mnmajor<128, 128>(kb, ks), sdesc_mnmajor<128, 128>(dsb, ks), idMN, ks > 0);
+      mma_commit(bar(C::B_DQFULL));
     }
     mma_commit(bar(C::B_FINAL));
     if (ok && tile_counter != nullptr) atomicAdd(tile_counter, static_cast<unsigned long long>(n_it));
-  } else if (warp == 2 && lane == 0 && !skip) {
-    // ---------------------------------------------------------------- dQ reducer
-    const uint32_t dqs = sb + C::OFF_DQ;
-    for (int j = 0; j < n_it; ++j) {
-      if (!mbar_wait(bar(C::B_DQSFULL), j & 1, guard, SITE_REDUCER)) break;
-      const int q0 = (i0 + j) * C::BM;
-      const int rows = min(C::BM, N - q0);
-      bulk_reduce_add_f32(dQacc + (row0 + q0) * C::D, dqs, static_cast<uint32_t>(rows * C::D * 4));
-      bulk_commit();
-      bulk_wait_read0();
-      mbar_arrive(bar(C::B_DQSEMPTY));
-    }
-    bulk_wait0();
   } else if (warp >= 4 && !skip) {
     // ---------------------------------------------------------------- element-wise warps
     const int qw = warp & 3;        // tensor-memory lane quarter
-    const int h = (warp - 4) >> 2;  // query half of each 64-row tile
+    const int h = (warp - 4) >> 2;  // query half (64 queries) of each tile
     const int kr = qw * 32 + lane;  // key row (tensor-memory lane); also the d index of dQ^T
     const int key = kt * C::BN + kr;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-    float* dQs = reinterpret_cast<float*>(smem + C::OFF_DQ);
     bool ok = true;
 
+    // dQ_j^T (lane = d, columns = queries) -> dQ workspace rows, 32 consecutive d per warp access
     auto read_dq = [&](int j) -> bool {
-      const int bj = j & 1;
-      if (!mbar_wait_warp(bar(C::B_DQFULL + bj), (j >> 1) & 1, guard, SITE_COMPUTE)) return false;
+      if (!mbar_wait_warp(bar(C::B_DQFULL), j & 1, guard, SITE_COMPUTE)) return false;
       tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(tl + C::TM_DP + 64 * bj + 32 * h, r);
-      tmem_ld_wait<32>(r);
+      uint32_t r[64];
+      tmem_ld32(tl + C::TM_DP + 64 * h, r);
+      tmem_ld32(tl + C::TM_DP + 64 * h + 32, r + 32);
+      tmem_ld_wait<64>(r);
       tc_fence_before();
-      mbar_arrive(bar(C::B_DQCONS + bj));
-      if (j >= 1 && !mbar_wait_warp(bar(C::B_DQSEMPTY), (j - 1) & 1, guard, SITE_COMPUTE)) return false;
+      mbar_arrive(bar(C::B_DQCONS));
+      const int qb = (i0 + j) * C::BM + 64 * h;
+      float* dst = dQacc + (row0 + qb) * C::D + kr;
+      const int nq = min(64, N - qb);
+      if (nq >= 64) {
 #pragma unroll
-      for (int x = 0; x < 32; ++x) dQs[(32 * h + x) * C::D + kr] = __uint_as_float(r[x]);
-      fence_proxy_async_smem();
-      mbar_arrive(bar(C::B_DQSFULL));
+        for (int x = 0; x < 64; ++x) atomicAdd(dst + static_cast<size_t>(x) * C::D, __uint_as_float(r[x]));
+      } else {
+#pragma unroll
+        for (int x = 0; x < 64; ++x)
+          if (x < nq) atomicAdd(dst + static_cast<size_t>(x) * C::D, __uint_as_float(r[x]));
+      }
       return true;
     };
 
     for (int it = 0; it < n_it; ++it) {
-      const int b = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!(ok = mbar_wait_warp(bar(C::B_QFULL + b), ph, guard, SITE_COMPUTE))) break;
-      if (!(ok = mbar_wait_warp(bar(C::B_SFULL + b), ph, guard, SITE_COMPUTE))) break;
-      if (!(ok = mbar_wait_warp(bar(C::B_DPFULL + b), ph, guard, SITE_COMPUTE))) break;
+      const int s = it & 1;
+      if (it > 0 && !(ok = read_dq(it - 1))) break;
+      if (!(ok = mbar_wait_warp(bar(C::B_QFULL + s), (it >> 1) & 1, guard, SITE_COMPUTE))) break;
+      if (!(ok = mbar_wait_warp(bar(C::B_SFULL), it & 1, guard, SITE_COMPUTE))) break;
       tc_fence_after();
-      uint32_t rs[32], rp[32];
-      tmem_ld32(tl + C::TM_S + 64 * b + 32 * h, rs);
-      tmem_ld32(tl + C::TM_DP + 64 * b + 32 * h, rp);
-      tmem_ld_wait<32>(rs);
-      tmem_ld_wait<32>(rp);
-      const int qh = (i0 + it) * C::BM + 32 * h;  // first query of this half
-      const float4* L4 = reinterpret_cast<const float4*>(smem + C::OFF_LD + b * C::LD_BYTES) + 8 * h;
+      const int qh = (i0 + it) * C::BM + 64 * h;  // first query of this half
+      const float4* L4 = reinterpret_cast<const float4*>(smem_raw + C::OFF_LD + s * C::LD_BYTES) + 16 * h;
       const float4* D4 = L4 + C::BM / 4;
       const bool masked = (CAUSAL && kt * C::BN + C::BN - 1 > qh) || (kt * C::BN + C::BN > N);
-      uint32_t pk[16], dk[16];
+      // ---- P^T = 2^(S^T c - L log2 e)
+      uint32_t pk[32];
+      {
+        uint32_t r[64];
+        tmem_ld32(tl + C::TM_S + 64 * h, r);
+        tmem_ld32(tl + C::TM_S + 64 * h + 32, r + 32);
+        tmem_ld_wait<64>(r);
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        const float4 l = L4[v], dd = D4[v];
-        const float lv[4] = {l.x, l.y, l.z, l.w}, dv[4] = {dd.x, dd.y, dd.z, dd.w};
-        float p[4], ds[4];
+        for (int v = 0; v < 16; ++v) {
+          const float4 l = L4[v];
+          const float lv[4] = {l.x, l.y, l.z, l.w};
+          float p[4];
 #pragma unroll
-        for (int y = 0; y < 4; ++y) {
-          const int x = 4 * v + y;
-          p[y] = ex2(fmaf(__uint_as_float(rs[x]), c_log2, -lv[y]));
-          if (masked && ((CAUSAL && key > qh + x) || key >= N)) p[y] = 0.f;
-          ds[y] = p[y] * (__uint_as_float(rp[x]) - dv[y]);
+          for (int y = 0; y < 4; ++y) {
+            const int x = 4 * v + y;
+            p[y] = ex2(fmaf(__uint_as_float(r[x]), c_log2, -lv[y]));
+            if (masked && ((CAUSAL && key > qh + x) || key >= N)) p[y] = 0.f;
+          }
+          pk[2 * v] = pack_bf16x2(p[0], p[1]);
+          pk[2 * v + 1] = pack_bf16x2(p[2], p[3]);
         }
-        pk[2 * v] = pack_bf16x2(p[0], p[1]);
-        pk[2 * v + 1] = pack_bf16x2(p[2], p[3]);
-        dk[2 * v] = pack_bf16x2(ds[0], ds[1]);
-        dk[2 * v + 1] = pack_bf16x2(ds[2], ds[3]);
       }
-      // P^T of these 32 queries over this half's own S^T columns
-      tmem_st16(tl + C::TM_S + 64 * b + 32 * h, pk);
-      // dS^T row kr, queries 32h .. 32h+31: four 16-byte units of a 128-byte swizzled row
-      uint8_t* row = smem + C::OFF_DS + b * C::DS_BYTES + kr * 128;
+      tmem_st32(tl + C::TM_S + 64 * h, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PREADY));
+      // ---- dS^T = P^T (dP^T - D), from the same bf16 P that enters dV
+      if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), it & 1, guard, SITE_COMPUTE))) break;
+      tc_fence_after();
+      uint32_t dk[32];
+      {
+        uint32_t r[64];
+        tmem_ld32(tl + C::TM_DP + 64 * h, r);
+        tmem_ld32(tl + C::TM_DP + 64 * h + 32, r + 32);
+        tmem_ld_wait<64>(r);
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        *reinterpret_cast<uint4*>(row + (((4 * h + u) ^ (kr & 7)) << 4)) =
+        for (int v = 0; v < 16; ++v) {
+          const float4 dd = D4[v];
+          const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
+          float ds[4];
+#pragma unroll
+          for (int y = 0; y < 4; ++y) {
+            const int x = 4 * v + y;
+            const uint32_t w = pk[x >> 1];
+            const float p = __uint_as_float((x & 1) ? (w & 0xffff0000u) : (w << 16));
+            ds[y] = p * (__uint_as_float(r[x]) - dv[y]);
+          }
+          dk[2 * v] = pack_bf16x2(ds[0], ds[1]);
+          dk[2 * v + 1] = pack_bf16x2(ds[2], ds[3]);
+        }
+      }
+      tmem_st32(tl + C::TM_S + 64 * h + 32, dk);
+      // dS^T row kr, queries 64h .. 64h+63: one 128-byte swizzled row of chunk h
+      uint8_t* row = tiles + C::T_DS + h * (128 * 128) + kr * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(row + ((u ^ (kr & 7)) << 4)) =
             make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(C::B_PREADY + b));
-      if (it >= 1 && !(ok = read_dq(it - 1))) break;
+      mbar_arrive(bar(C::B_DSREADY));
     }
     if (ok && n_it > 0) ok = read_dq(n_it - 1);
     // dK (times scale) and dV: this warp's lane quarter, d columns 64h .. 64h+63

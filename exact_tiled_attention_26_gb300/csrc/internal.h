@@ -13,7 +13,7 @@ namespace fa {
 // Tile shapes (see fa_get_tile_config).
 constexpr int kFwdBr = 128, kFwdBc = 128;
 constexpr int kBwdBc = 128;
-constexpr int bwd_br(int d) { return d == 128 ? 64 : 128; }
+constexpr int bwd_br(int) { return 128; }
 
 // Device status word of the current device (see fa_poll_device_error).
 int* device_status_word();

@@ -86,7 +86,7 @@ def test_workspace_size(fa_lib):
 
 def test_tile_config(fa_lib):
     assert fa_lib.fa_get_tile_config(128, 0) == (0, 128, 128)
-    assert fa_lib.fa_get_tile_config(128, 1) == (0, 64, 128)
+    assert fa_lib.fa_get_tile_config(128, 1) == (0, 128, 128)
     assert fa_lib.fa_get_tile_config(64, 1) == (0, 128, 128)
     assert fa_lib.fa_get_tile_config(32, 1) == (0, 128, 128)
     assert fa_lib.fa_get_tile_config(100, 0)[0] == fa_lib.FA_ERR_UNSUPPORTED
