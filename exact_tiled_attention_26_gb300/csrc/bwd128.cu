@@ -28,7 +28,12 @@
 // Warps: 0 TMA producer (its 32 lanes also stage L*log2 e and D of each query
 // tile in shared memory, two tiles ahead), 1 UMMA issuer (one thread), 4..11
 // element-wise (warp w: tensor-memory lane quarter w % 4, query half (w - 4) / 4;
-// one key row per thread, which is also the d index of dQ^T).
+// one key row per thread), 12..15 dQ drain (warp w: lane quarter w % 4, i.e. 32
+// values of d; each takes all 128 columns of dQ^T out of tensor memory at once,
+// frees the columns, then issues the reductions while the next step runs).  L2
+// absorbs fp32 reductions at about 20 bytes per clock per SM, so the 64 KiB of
+// dQ per step are drained off the element-wise warps' path.  Registers move from
+// the producer/UMMA warpgroup to the others with setmaxnreg: 72 + 3 x 144 <= 4 x 128.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -39,8 +44,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct B128 {
   static constexpr int D = 128, BN = 128, BM = 128;
-  static constexpr int NTHREADS = 384;
+  static constexpr int NTHREADS = 512;
   static constexpr int NCOMP = 256;             // element-wise threads
+  static constexpr int NDQ = 128;               // dQ drain threads
   static constexpr int TILE = 128 * 128 * 2;    // one 128 x 128 bf16 tile (two 64-column chunks)
   // small region at the start of dynamic shared memory
   enum : int {
@@ -106,7 +112,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     mbar_init(bar(C::B_DSREADY), C::NCOMP);
     mbar_init(bar(C::B_DKDONE), 1);
     mbar_init(bar(C::B_DQFULL), 1);
-    mbar_init(bar(C::B_DQCONS), C::NCOMP);
+    mbar_init(bar(C::B_DQCONS), C::NDQ);
     mbar_init(bar(C::B_FINAL), 1);
     *abort_flag = (*reinterpret_cast<volatile int*>(status) != 0);
     fence_mbar_init();
@@ -126,6 +132,9 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
   const uint32_t tmem = *tmem_slot;
   const bool skip = *abort_flag != 0;
 
+  if (warp < 4) {
+  // warpgroup 0 gives registers to the others; warps 2 and 3 have no role
+  regs_dec<72>();
   if (warp == 0 && !skip) {
     // ---------------------------------------------------------------- producer (whole warp)
     if (lane == 0) {
@@ -219,7 +228,41 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     }
     mma_commit(bar(C::B_FINAL));
     if (ok && tile_counter != nullptr) atomicAdd(tile_counter, static_cast<unsigned long long>(n_it));
-  } else if (warp >= 4 && !skip) {
+  }
+  } else if (warp >= 12) {
+    regs_inc<144>();
+    if (!skip) {
+    // ---------------------------------------------------------------- dQ drain
+    // dQ_j^T (lane = d, columns = queries) -> dQ workspace rows; each warp access
+    // covers 32 consecutive d of one query row (128 bytes).
+    const int qw = warp & 3;
+    const int dd = qw * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    for (int j = 0; j < n_it; ++j) {
+      if (!mbar_wait_warp(bar(C::B_DQFULL), j & 1, guard, SITE_COMPUTE)) break;
+      tc_fence_after();
+      uint32_t r[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tl + C::TM_DP + 32 * c, r + 32 * c);
+      tmem_ld_wait<128>(r);
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DQCONS));
+      const int q0 = (i0 + j) * C::BM;
+      float* dst = dQacc + (row0 + q0) * C::D + dd;
+      const int nq = min(C::BM, N - q0);
+      if (nq >= C::BM) {
+#pragma unroll
+        for (int x = 0; x < C::BM; ++x) atomicAdd(dst + static_cast<size_t>(x) * C::D, __uint_as_float(r[x]));
+      } else {
+#pragma unroll
+        for (int x = 0; x < C::BM; ++x)
+          if (x < nq) atomicAdd(dst + static_cast<size_t>(x) * C::D, __uint_as_float(r[x]));
+      }
+    }
+    }
+  } else {
+    regs_inc<144>();
+    if (!skip) {
     // ---------------------------------------------------------------- element-wise warps
     const int qw = warp & 3;        // tensor-memory lane quarter
     const int h = (warp - 4) >> 2;  // query half (64 queries) of each tile
@@ -228,33 +271,8 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
     bool ok = true;
 
-    // dQ_j^T (lane = d, columns = queries) -> dQ workspace rows, 32 consecutive d per warp access
-    auto read_dq = [&](int j) -> bool {
-      if (!mbar_wait_warp(bar(C::B_DQFULL), j & 1, guard, SITE_COMPUTE)) return false;
-      tc_fence_after();
-      uint32_t r[64];
-      tmem_ld32(tl + C::TM_DP + 64 * h, r);
-      tmem_ld32(tl + C::TM_DP + 64 * h + 32, r + 32);
-      tmem_ld_wait<64>(r);
-      tc_fence_before();
-      mbar_arrive(bar(C::B_DQCONS));
-      const int qb = (i0 + j) * C::BM + 64 * h;
-      float* dst = dQacc + (row0 + qb) * C::D + kr;
-      const int nq = min(64, N - qb);
-      if (nq >= 64) {
-#pragma unroll
-        for (int x = 0; x < 64; ++x) atomicAdd(dst + static_cast<size_t>(x) * C::D, __uint_as_float(r[x]));
-      } else {
-#pragma unroll
-        for (int x = 0; x < 64; ++x)
-          if (x < nq) atomicAdd(dst + static_cast<size_t>(x) * C::D, __uint_as_float(r[x]));
-      }
-      return true;
-    };
-
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
-      if (it > 0 && !(ok = read_dq(it - 1))) break;
       if (!(ok = mbar_wait_warp(bar(C::B_QFULL + s), (it >> 1) & 1, guard, SITE_COMPUTE))) break;
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL), it & 1, guard, SITE_COMPUTE))) break;
       tc_fence_after();
@@ -264,20 +282,20 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       const bool masked = (CAUSAL && kt * C::BN + C::BN - 1 > qh) || (kt * C::BN + C::BN > N);
       // ---- P^T = 2^(S^T c - L log2 e)
       uint32_t pk[32];
-      {
-        uint32_t r[64];
-        tmem_ld32(tl + C::TM_S + 64 * h, r);
-        tmem_ld32(tl + C::TM_S + 64 * h + 32, r + 32);
-        tmem_ld_wait<64>(r);
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::TM_S + 64 * h + 32 * half, r);
+        tmem_ld_wait<32>(r);
+#pragma unroll
+        for (int v = 8 * half; v < 8 * half + 8; ++v) {
           const float4 l = L4[v];
           const float lv[4] = {l.x, l.y, l.z, l.w};
           float p[4];
 #pragma unroll
           for (int y = 0; y < 4; ++y) {
             const int x = 4 * v + y;
-            p[y] = ex2(fmaf(__uint_as_float(r[x]), c_log2, -lv[y]));
+            p[y] = ex2(fmaf(__uint_as_float(r[x - 32 * half]), c_log2, -lv[y]));
             if (masked && ((CAUSAL && key > qh + x) || key >= N)) p[y] = 0.f;
           }
           pk[2 * v] = pack_bf16x2(p[0], p[1]);
@@ -292,13 +310,13 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), it & 1, guard, SITE_COMPUTE))) break;
       tc_fence_after();
       uint32_t dk[32];
-      {
-        uint32_t r[64];
-        tmem_ld32(tl + C::TM_DP + 64 * h, r);
-        tmem_ld32(tl + C::TM_DP + 64 * h + 32, r + 32);
-        tmem_ld_wait<64>(r);
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::TM_DP + 64 * h + 32 * half, r);
+        tmem_ld_wait<32>(r);
+#pragma unroll
+        for (int v = 8 * half; v < 8 * half + 8; ++v) {
           const float4 dd = D4[v];
           const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
           float ds[4];
@@ -307,7 +325,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
             const int x = 4 * v + y;
             const uint32_t w = pk[x >> 1];
             const float p = __uint_as_float((x & 1) ? (w & 0xffff0000u) : (w << 16));
-            ds[y] = p * (__uint_as_float(r[x]) - dv[y]);
+            ds[y] = p * (__uint_as_float(r[x - 32 * half]) - dv[y]);
           }
           dk[2 * v] = pack_bf16x2(ds[0], ds[1]);
           dk[2 * v + 1] = pack_bf16x2(ds[2], ds[3]);
@@ -325,7 +343,6 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       tc_fence_before();
       mbar_arrive(bar(C::B_DSREADY));
     }
-    if (ok && n_it > 0) ok = read_dq(n_it - 1);
     // dK (times scale) and dV: this warp's lane quarter, d columns 64h .. 64h+63
     if (ok) ok = mbar_wait_warp(bar(C::B_FINAL), 0, guard, SITE_COMPUTE);
     if (ok) {
@@ -350,6 +367,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
           }
         }
       }
+    }
     }
   }
 

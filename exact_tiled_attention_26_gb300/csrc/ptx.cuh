@@ -91,6 +91,12 @@ FA_DEV void mbar_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitL
   }
 }
 
+// Move registers between warpgroups (all four warps of a warpgroup execute it).
+template <uint32_t N>
+FA_DEV void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N)); }
+template <uint32_t N>
+FA_DEV void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N)); }
+
 FA_DEV void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
