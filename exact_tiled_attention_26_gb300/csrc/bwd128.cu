@@ -34,6 +34,8 @@
 // absorbs fp32 reductions at about 20 bytes per clock per SM, so the 64 KiB of
 // dQ per step are drained off the element-wise warps' path.  Registers move from
 // the producer/UMMA warpgroup to the others with setmaxnreg: 72 + 3 x 144 <= 4 x 128.
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -55,7 +57,7 @@ struct B128 {
   };
   static constexpr int OFF_BAR = 0;
   static constexpr int OFF_MISC = NBAR * 8;     // tensor-memory base, abort flag
-  static constexpr int OFF_LD = 256;            // 2 stages x (L*log2 e [128], D [128])
+  static constexpr int OFF_LD = 256;            // 2 stages x (-L*log2 e [128], D [128])
   static constexpr int LD_BYTES = 2 * BM * 4;
   static constexpr int SMALL = OFF_LD + 2 * LD_BYTES;
   // 1 KiB-aligned tiles after it
@@ -148,13 +150,13 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
       const int q0 = (i0 + it) * C::BM;
-      // L (times log2 e) and D of this query tile, read before waiting for the stage;
-      // rows past N get L = +inf so that their P is exactly 0
+      // -L log2 e and D of this query tile, read before waiting for the stage; rows
+      // past N get -L log2 e = -inf so that their P is exactly 0
       float lv[4], dv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int q = q0 + lane + 32 * u;
-        lv[u] = q < N ? Lg[row0 + q] * kLog2e : INFINITY;
+        lv[u] = q < N ? -Lg[row0 + q] * kLog2e : -INFINITY;
         dv[u] = q < N ? Dg[row0 + q] : 0.f;
       }
       if (!mbar_wait_warp(bar(C::B_QEMPTY + s), ((it >> 1) & 1) ^ 1, guard, SITE_PRODUCER)) break;
@@ -280,27 +282,39 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       const float4* L4 = reinterpret_cast<const float4*>(smem_raw + C::OFF_LD + s * C::LD_BYTES) + 16 * h;
       const float4* D4 = L4 + C::BM / 4;
       const bool masked = (CAUSAL && kt * C::BN + C::BN - 1 > qh) || (kt * C::BN + C::BN > N);
-      // ---- P^T = 2^(S^T c - L log2 e)
+      const uint64_t cc = f2pack(c_log2, c_log2);
+      // ---- P^T = 2^(S^T c - L log2 e), two columns per packed FMA
       uint32_t pk[32];
+      {
+        uint32_t r[64];
+        tmem_ld32(tl + C::TM_S + 64 * h, r);
+        tmem_ld32(tl + C::TM_S + 64 * h + 32, r + 32);
+        tmem_ld_wait<64>(r);
+        auto body = [&](auto mask_tag) {
+          constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(tl + C::TM_S + 64 * h + 32 * half, r);
-        tmem_ld_wait<32>(r);
+          for (int v = 0; v < 16; ++v) {
+            const float4 l = L4[v];
+            float p[4];
 #pragma unroll
-        for (int v = 8 * half; v < 8 * half + 8; ++v) {
-          const float4 l = L4[v];
-          const float lv[4] = {l.x, l.y, l.z, l.w};
-          float p[4];
-#pragma unroll
-          for (int y = 0; y < 4; ++y) {
-            const int x = 4 * v + y;
-            p[y] = ex2(fmaf(__uint_as_float(r[x - 32 * half]), c_log2, -lv[y]));
-            if (masked && ((CAUSAL && key > qh + x) || key >= N)) p[y] = 0.f;
+            for (int y = 0; y < 4; y += 2) {
+              const int x = 4 * v + y;
+              const uint64_t t = ffma2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), cc,
+                                       y == 0 ? f2pack(l.x, l.y) : f2pack(l.z, l.w));
+              float t0, t1;
+              f2unpack(t, t0, t1);
+              p[y] = ex2(t0);
+              p[y + 1] = ex2(t1);
+              if (MASK) {
+                if ((CAUSAL && key > qh + x) || key >= N) p[y] = 0.f;
+                if ((CAUSAL && key > qh + x + 1) || key >= N) p[y + 1] = 0.f;
+              }
+            }
+            pk[2 * v] = pack_bf16x2(p[0], p[1]);
+            pk[2 * v + 1] = pack_bf16x2(p[2], p[3]);
           }
-          pk[2 * v] = pack_bf16x2(p[0], p[1]);
-          pk[2 * v + 1] = pack_bf16x2(p[2], p[3]);
-        }
+        };
+        if (masked) body(std::true_type{}); else body(std::false_type{});
       }
       tmem_st32(tl + C::TM_S + 64 * h, pk);
       tmem_st_wait();
@@ -310,25 +324,25 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), it & 1, guard, SITE_COMPUTE))) break;
       tc_fence_after();
       uint32_t dk[32];
+      {
+        uint32_t r[64];
+        tmem_ld32(tl + C::TM_DP + 64 * h, r);
+        tmem_ld32(tl + C::TM_DP + 64 * h + 32, r + 32);
+        tmem_ld_wait<64>(r);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        tmem_ld32(tl + C::TM_DP + 64 * h + 32 * half, r);
-        tmem_ld_wait<32>(r);
-#pragma unroll
-        for (int v = 8 * half; v < 8 * half + 8; ++v) {
+        for (int v = 0; v < 16; ++v) {
           const float4 dd = D4[v];
-          const float dv[4] = {dd.x, dd.y, dd.z, dd.w};
-          float ds[4];
 #pragma unroll
-          for (int y = 0; y < 4; ++y) {
+          for (int y = 0; y < 4; y += 2) {
             const int x = 4 * v + y;
             const uint32_t w = pk[x >> 1];
-            const float p = __uint_as_float((x & 1) ? (w & 0xffff0000u) : (w << 16));
-            ds[y] = p * (__uint_as_float(r[x - 32 * half]) - dv[y]);
+            const uint64_t pp = f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+            const uint64_t t = fadd2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])),
+                                     y == 0 ? f2pack(-dd.x, -dd.y) : f2pack(-dd.z, -dd.w));
+            float d0, d1;
+            f2unpack(fmul2(pp, t), d0, d1);
+            dk[x >> 1] = pack_bf16x2(d0, d1);
           }
-          dk[2 * v] = pack_bf16x2(ds[0], ds[1]);
-          dk[2 * v + 1] = pack_bf16x2(ds[2], ds[3]);
         }
       }
       tmem_st32(tl + C::TM_S + 64 * h + 32, dk);
