@@ -9,9 +9,13 @@
 //
 // One CTA owns one 128-row query tile of one (batch, head).  Warp roles:
 //   warp 0      TMA producer: Q once, then a 2-stage ring of K and V tiles
-//   warp 1      UMMA issuer (one thread): S_j = Q K_j^T into tensor memory
-//               (three buffers), O += P_{j-1} V_{j-1} with P read from
-//               tensor memory
+//   warp 1      UMMA issuer of S_j = Q K_j^T (one thread) into tensor memory
+//               (three buffers)
+//   warp 2      UMMA issuer of O += P_j V_j (one thread), P read from tensor
+//               memory.  Two issuing threads keep the tensor pipe fed while
+//               either waits on a barrier: a wait costs the issuing thread about
+//               a hundred cycles even when the barrier is already complete, and
+//               the pipe's queue of UMMAs is too short to cover that.
 //   warps 4..7  softmax: one thread per query row (its tensor-memory lane);
 //               online max/sum in base 2 with the scale folded into one FMA,
 //               P written back as bf16 over its own S columns; epilogue
@@ -44,7 +48,7 @@ struct FwdCfg {
   static constexpr int NSB = 3;  // S/P buffers in tensor memory
   // barriers
   static constexpr int B_Q = 0, B_KFULL = 1, B_KEMPTY = 3, B_VFULL = 5, B_VEMPTY = 7, B_SFULL = 9,
-                       B_PFULL = 12, B_PFREE = 15, B_OSTEP = 18, B_OFINAL = 19, NBAR = 20;
+                       B_PFULL = 12, B_PFREE = 15, B_OFINAL = 18, B_SDONE = 19, NBAR = 20;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_USED = OFF_MISC + 16;
   // ask for enough that only one CTA fits per SM (each CTA holds all 512 TMEM columns)
@@ -91,8 +95,8 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(bar(C::B_PFULL + b), 128);
       mbar_init(bar(C::B_PFREE + b), 1);
     }
-    mbar_init(bar(C::B_OSTEP), 1);
     mbar_init(bar(C::B_OFINAL), 1);
+    mbar_init(bar(C::B_SDONE), 1);
     // an earlier launch gave up: do no work until the host has polled the status
     *abort_flag = (*reinterpret_cast<volatile int*>(status) != 0);
     fence_mbar_init();
@@ -140,44 +144,45 @@ __global__ void __launch_bounds__(256, 1)
       for (int j = (jv > 0 ? jv - 1 : 0); j <= jv; ++j) mbar_drain(bar(C::B_VFULL + (j & 1)), (j >> 1) & 1);
     }
   } else if (warp == 1 && lane == 0 && !skip) {
-    // ---------------------------------------------------------------- UMMA issuer
+    // ---------------------------------------------------------------- UMMA issuer: S
     constexpr uint32_t idS = idesc_bf16(128, C::BN, false, false);  // Q (K-major) x K (K-major)
-    constexpr uint32_t idO = idesc_bf16(128, D, false, true);       // P (tensor memory) x V (N-major)
     bool ok = mbar_wait(bar(C::B_Q), 0, guard, SITE_FWD_MMA);
-    for (int j = 0; ok && j <= n_kv; ++j) {
-      if (j < n_kv) {
-        const int s = j & 1, b = j % C::NSB;
-        // S buffer b last held P_{j-3}: the product that read it must be done
-        if (j >= C::NSB && !(ok = mbar_wait(bar(C::B_PFREE + b), ((j / C::NSB) & 1) ^ 1, guard, SITE_FWD_MMA)))
-          break;
-        if (!(ok = mbar_wait(bar(C::B_KFULL + s), (j >> 1) & 1, guard, SITE_FWD_MMA))) break;
-        tc_fence_after();
-        const uint32_t kb = sb + C::OFF_K + s * C::TILE;
-        const uint32_t dS = tmem + C::TM_S0 + b * 128;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j & 1, b = j % C::NSB;
+      // S buffer b last held P_{j-3}: the product that read it must be done
+      if (j >= C::NSB && !(ok = mbar_wait(bar(C::B_PFREE + b), ((j / C::NSB) & 1) ^ 1, guard, SITE_FWD_MMA)))
+        break;
+      if (!(ok = mbar_wait(bar(C::B_KFULL + s), (j >> 1) & 1, guard, SITE_FWD_MMA))) break;
+      tc_fence_after();
+      const uint32_t kb = sb + C::OFF_K + s * C::TILE;
+      const uint32_t dS = tmem + C::TM_S0 + b * 128;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(dS, sdesc_kmajor<C::SWB, C::BM>(sb + C::OFF_Q, ks), sdesc_kmajor<C::SWB, C::BN>(kb, ks), idS,
-                 ks > 0);
-        mma_commit(bar(C::B_SFULL + b));
-        mma_commit(bar(C::B_KEMPTY + s));
-      }
-      if (j >= 1) {
-        const int jj = j - 1, s = jj & 1, b = jj % C::NSB;
-        if (!(ok = mbar_wait(bar(C::B_PFULL + b), (jj / C::NSB) & 1, guard, SITE_FWD_MMA))) break;
-        if (!(ok = mbar_wait(bar(C::B_VFULL + s), (jj >> 1) & 1, guard, SITE_FWD_MMA))) break;
-        tc_fence_after();
-        const uint32_t vb = sb + C::OFF_V + s * C::TILE;
-        const uint32_t aP = tmem + C::TM_S0 + b * 128;  // bf16 P packed two per column
-#pragma unroll
-        for (int ks = 0; ks < C::BN / 16; ++ks)
-          mma_ts(tmem + C::TM_O, aP + ks * 8, sdesc_mnmajor<C::SWB, C::BN>(vb, ks), idO, (jj > 0 || ks > 0));
-        mma_commit(bar(C::B_VEMPTY + s));
-        mma_commit(bar(C::B_PFREE + b));
-        mma_commit(bar(C::B_OSTEP));
-      }
+      for (int ks = 0; ks < D / 16; ++ks)
+        mma_ss(dS, sdesc_kmajor<C::SWB, C::BM>(sb + C::OFF_Q, ks), sdesc_kmajor<C::SWB, C::BN>(kb, ks), idS, ks > 0);
+      mma_commit(bar(C::B_SFULL + b));
+      mma_commit(bar(C::B_KEMPTY + s));
     }
-    mma_commit(bar(C::B_OFINAL));  // also the drain point for teardown
+    mma_commit(bar(C::B_SDONE));  // drain point for teardown
     if (ok && tile_counter != nullptr) atomicAdd(tile_counter, static_cast<unsigned long long>(n_kv));
+  } else if (warp == 2 && lane == 0 && !skip) {
+    // ---------------------------------------------------------------- UMMA issuer: P V
+    constexpr uint32_t idO = idesc_bf16(128, D, false, true);  // P (tensor memory) x V (N-major)
+    bool ok = true;
+    for (int jj = 0; jj < n_kv; ++jj) {
+      const int s = jj & 1, b = jj % C::NSB;
+      if (!(ok = mbar_wait(bar(C::B_PFULL + b), (jj / C::NSB) & 1, guard, SITE_FWD_MMA))) break;
+      if (!(ok = mbar_wait(bar(C::B_VFULL + s), (jj >> 1) & 1, guard, SITE_FWD_MMA))) break;
+      tc_fence_after();
+      const uint32_t vb = sb + C::OFF_V + s * C::TILE;
+      const uint32_t aP = tmem + C::TM_S0 + b * 128;  // bf16 P packed two per column
+#pragma unroll
+      for (int ks = 0; ks < C::BN / 16; ++ks)
+        mma_ts(tmem + C::TM_O, aP + ks * 8, sdesc_mnmajor<C::SWB, C::BN>(vb, ks), idO, (jj > 0 || ks > 0));
+      mma_commit(bar(C::B_VEMPTY + s));
+      mma_commit(bar(C::B_PFREE + b));
+    }
+    // every S_j completed before P_j existed, so this also marks the end of all UMMAs
+    mma_commit(bar(C::B_OFINAL));
   } else if (warp >= 4 && !skip) {
     // ---------------------------------------------------------------- softmax + epilogue
     const int wq = warp & 3;
@@ -222,8 +227,11 @@ __global__ void __launch_bounds__(256, 1)
             lr_run *= alpha;
             m_run = m_tile;
           }
-          // O holds P_0..P_{j-1} V: wait for the last of those products
-          if (!(ok = mbar_wait_warp(bar(C::B_OSTEP), (j - 1) & 1, guard, SITE_FWD_SOFTMAX))) break;
+          // O holds P_0..P_{j-1} V: wait for the last of those products.  Its barrier
+          // is the one that frees S buffer (j-1) % 3; PV_{j-3} is already done (S_j
+          // waited for it), so that barrier is at most one phase behind.
+          const int pb = (j - 1) % C::NSB;
+          if (!(ok = mbar_wait_warp(bar(C::B_PFREE + pb), ((j - 1) / C::NSB) & 1, guard, SITE_FWD_SOFTMAX))) break;
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -290,7 +298,10 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 1) {
     if (!skip && *abort_flag) {
       // gave up: make sure no UMMA is still writing tensor memory before freeing it
-      if (lane == 0) mbar_drain(bar(C::B_OFINAL), 0);
+      if (lane == 0) {
+        mbar_drain(bar(C::B_SDONE), 0);
+        mbar_drain(bar(C::B_OFINAL), 0);
+      }
       __syncwarp();
     }
     tc_fence_after();

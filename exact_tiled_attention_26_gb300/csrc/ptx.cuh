@@ -221,6 +221,27 @@ FA_DEV uint64_t sdesc_mnmajor(uint32_t base, int ks) {
   return make_sdesc(addr, ROWS * SWB, 8 * SWB, SwzCode<SWB>::v);
 }
 
+// The same descriptors as a base (k-step 0) plus a per-k-step byte offset, so
+// that an issuing loop adds a compile-time constant to the start-address field
+// (bits [0,14), address >> 4) instead of rebuilding the descriptor.
+template <int SWB, int ROWS>
+FA_DEV uint64_t sdesc_kmajor_base(uint32_t base) {
+  return make_sdesc(base, 16, 8 * SWB, SwzCode<SWB>::v);
+}
+template <int SWB, int ROWS>
+FA_DEV uint64_t sdesc_mnmajor_base(uint32_t base) {
+  return make_sdesc(base, ROWS * SWB, 8 * SWB, SwzCode<SWB>::v);
+}
+template <int SWB, int ROWS>
+__host__ __device__ constexpr uint32_t kmajor_off(int ks) {
+  return static_cast<uint32_t>(((ks * 16) / (SWB / 2)) * (ROWS * SWB) + ((ks * 16) % (SWB / 2)) * 2);
+}
+template <int SWB>
+__host__ __device__ constexpr uint32_t mnmajor_off(int ks) {
+  return static_cast<uint32_t>(ks * 16 * SWB);
+}
+FA_DEV uint64_t desc_at(uint64_t base_desc, uint32_t byte_off) { return base_desc + (byte_off >> 4); }
+
 // Byte offset of bf16 element (row, col) in a SWB=128 tile written as above
 // (ROWS rows per chunk), including the 128-byte swizzle (16-byte unit index
 // XOR row % 8).  The tile base must be 1024-byte aligned.
@@ -290,6 +311,12 @@ FA_DEV float lg2(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+FA_DEV float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Packed pairs of fp32 (Blackwell's two-wide FP32 instructions).
 FA_DEV uint64_t f2pack(float lo, float hi) {
   uint64_t r;
