@@ -26,7 +26,9 @@
 // dV) and hand dQ to L2 (during the next S).
 //
 // Warps: 0 TMA producer (its 32 lanes also stage L*log2 e and D of each query
-// tile in shared memory, two tiles ahead), 1 UMMA issuer (one thread), 4..11
+// tile in shared memory, two tiles ahead), 1 and 2 UMMA issuers (one thread
+// each: S^T and dP^T; dV, dK and dQ^T -- two issuing threads keep the tensor pipe
+// fed while either one waits on a barrier), 4..11
 // element-wise (warp w: tensor-memory lane quarter w % 4, query half (w - 4) / 4;
 // one key row per thread), 12..15 dQ drain (warp w: lane quarter w % 4, i.e. 32
 // values of d; each takes all 128 columns of dQ^T out of tensor memory at once,
@@ -53,7 +55,7 @@ struct B128 {
   // small region at the start of dynamic shared memory
   enum : int {
     B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6, B_PREADY = 7, B_DSREADY = 8, B_DKDONE = 9,
-    B_DQFULL = 10, B_DQCONS = 11, B_FINAL = 12, NBAR = 13
+    B_DQFULL = 10, B_DQCONS = 11, B_FINAL = 12, B_ADONE = 13, NBAR = 14
   };
   static constexpr int OFF_BAR = 0;
   static constexpr int OFF_MISC = NBAR * 8;     // tensor-memory base, abort flag
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQCONS), C::NDQ);
     mbar_init(bar(C::B_FINAL), 1);
+    mbar_init(bar(C::B_ADONE), 1);
     *abort_flag = (*reinterpret_cast<volatile int*>(status) != 0);
     fence_mbar_init();
   }
@@ -182,11 +185,9 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
         mbar_drain(bar(C::B_QFULL + (it & 1)), (it >> 1) & 1);
     }
   } else if (warp == 1 && lane == 0 && !skip) {
-    // ---------------------------------------------------------------- UMMA issuer
+    // ---------------------------------------------------------------- UMMA issuer A: S^T, dP^T
     constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // S^T, dP^T: K-major x K-major
-    constexpr uint32_t idTN = idesc_bf16(128, 128, false, true);   // dV, dK: A in TMEM x N-major B
-    constexpr uint32_t idMN = idesc_bf16(128, 128, true, true);    // dQ^T: K^T (M-major) x dS^T (N-major)
-    const uint32_t kb = tb + C::T_K, vb = tb + C::T_V, dsb = tb + C::T_DS;
+    const uint32_t kb = tb + C::T_K, vb = tb + C::T_V;
     bool ok = mbar_wait(bar(C::B_KV), 0, guard, SITE_MMA);
     for (int it = 0; ok && it < n_it; ++it) {
       const int s = it & 1;
@@ -206,6 +207,20 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       for (int ks = 0; ks < 8; ++ks)
         mma_ss(tmem + C::TM_DP, sdesc_kmajor<128, 128>(vb, ks), sdesc_kmajor<128, 128>(db, ks), idKK, ks > 0);
       mma_commit(bar(C::B_DPFULL));
+    }
+    mma_commit(bar(C::B_ADONE));  // drain point for teardown
+    if (ok && tile_counter != nullptr) atomicAdd(tile_counter, static_cast<unsigned long long>(n_it));
+  } else if (warp == 2 && lane == 0 && !skip) {
+    // ---------------------------------------------------------------- UMMA issuer B: dV, dK, dQ^T
+    // S^T and dP^T of a step are complete before the element-wise warps can signal
+    // P and dS ready, so this thread's commits cover every reader of Q_i and dO_i.
+    constexpr uint32_t idTN = idesc_bf16(128, 128, false, true);  // dV, dK: A in TMEM x N-major B
+    constexpr uint32_t idMN = idesc_bf16(128, 128, true, true);   // dQ^T: K^T (M-major) x dS^T (N-major)
+    const uint32_t kb = tb + C::T_K, dsb = tb + C::T_DS;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1;
+      const uint32_t qb = tb + C::T_Q + s * 2 * C::TILE, db = tb + C::T_DO + s * 2 * C::TILE;
       // dV += P^T dO_i  (P^T of query block ks: half ks/4, columns (ks%4)*8 of it)
       if (!(ok = mbar_wait(bar(C::B_PREADY), it & 1, guard, SITE_MMA))) break;
       tc_fence_after();
@@ -229,7 +244,6 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       mma_commit(bar(C::B_DQFULL));
     }
     mma_commit(bar(C::B_FINAL));
-    if (ok && tile_counter != nullptr) atomicAdd(tile_counter, static_cast<unsigned long long>(n_it));
   }
   } else if (warp >= 12) {
     regs_inc<144>();
@@ -389,7 +403,10 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
   __syncthreads();
   if (warp == 1) {
     if (!skip && *abort_flag) {
-      if (lane == 0) mbar_drain(bar(C::B_FINAL), 0);
+      if (lane == 0) {
+        mbar_drain(bar(C::B_ADONE), 0);
+        mbar_drain(bar(C::B_FINAL), 0);
+      }
       __syncwarp();
     }
     tc_fence_after();
