@@ -37,6 +37,13 @@ METRIC = "attention fwd+bwd TFLOP/s (bf16, d=128, N=4K-32K)"
 UNIT = "TFLOP/s"
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
+# backward main kernel, from the ncu capture summarised in
+# profiles/launches_vlong_1x32x32768x128_causal.md; valid for the kernel as captured
+# there (set to None whenever the kernel changes).
+_TRAFFIC = {("vlong_1x32x32768x128", True): 1620613888 + 1022937088}
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -272,9 +279,10 @@ def run_ours(args):
         "frac_of_bf16_peak": round(value / world / sustained, 4),
         "roofline": {
             "bound": "tensor",
-            "kernel": "fa_bwd (bwd main kernel, with its workspace memset and dQ convert)",
+            "kernel": "bwd_d128_kernel (timed as the fa_bwd call: main kernel + workspace clear + dQ convert)",
             "achieved": round(bwd_tflops, 2), "peak": sustained, "unit": "TFLOP/s",
-            "frac": round(bwd_tflops / sustained, 4), "traffic": None,
+            "frac": round(bwd_tflops / sustained, 4),
+            "traffic": _TRAFFIC.get((w.name, causal)),
             "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
             "algorithmic": "10 N^2 d / 2 FLOPs per head (causal) per launch",
         },
