@@ -54,8 +54,8 @@ struct B128 {
   static constexpr int TILE = 128 * 128 * 2;    // one 128 x 128 bf16 tile (two 64-column chunks)
   // small region at the start of dynamic shared memory
   enum : int {
-    B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6, B_PREADY = 7, B_DSREADY = 8, B_DKDONE = 9,
-    B_DQFULL = 10, B_DQCONS = 11, B_FINAL = 12, B_ADONE = 13, NBAR = 14
+    B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6, B_PREADY = 7, B_DSREADY = 9, B_DKDONE = 11,
+    B_DQFULL = 12, B_DQCONS = 13, B_FINAL = 14, B_ADONE = 15, NBAR = 16
   };
   static constexpr int OFF_BAR = 0;
   static constexpr int OFF_MISC = NBAR * 8;     // tensor-memory base, abort flag
@@ -112,8 +112,10 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
-    mbar_init(bar(C::B_PREADY), C::NCOMP);
-    mbar_init(bar(C::B_DSREADY), C::NCOMP);
+    for (int c = 0; c < 2; ++c) {  // the two 32-query sub-chunks of each thread's 64 queries
+      mbar_init(bar(C::B_PREADY + c), C::NCOMP);
+      mbar_init(bar(C::B_DSREADY + c), C::NCOMP);
+    }
     mbar_init(bar(C::B_DKDONE), 1);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQCONS), C::NDQ);
@@ -221,20 +223,34 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
       const uint32_t qb = tb + C::T_Q + s * 2 * C::TILE, db = tb + C::T_DO + s * 2 * C::TILE;
-      // dV += P^T dO_i  (P^T of query block ks: half ks/4, columns (ks%4)*8 of it)
-      if (!(ok = mbar_wait(bar(C::B_PREADY), it & 1, guard, SITE_MMA))) break;
-      tc_fence_after();
+      // dV += P^T dO_i.  Query block ks (16 queries) is in half ks/4, sub-chunk (ks%4)/2;
+      // its bf16 P^T sits in columns 64 (ks/4) + 8 (ks%4).  Sub-chunk 0 (blocks 0,1,4,5)
+      // is ready before sub-chunk 1 (blocks 2,3,6,7).
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_ts(tmem + C::TM_DV, tmem + C::TM_S + 64 * (ks >> 2) + (ks & 3) * 8, sdesc_mnmajor<128, 128>(db, ks),
-               idTN, (it > 0 || ks > 0));
-      // dK += dS^T Q_i
-      if (!(ok = mbar_wait(bar(C::B_DSREADY), it & 1, guard, SITE_MMA))) break;
-      tc_fence_after();
+      for (int c = 0; c < 2; ++c) {
+        if (!(ok = mbar_wait(bar(C::B_PREADY + c), it & 1, guard, SITE_MMA))) break;
+        tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_ts(tmem + C::TM_DK, tmem + C::TM_S + 64 * (ks >> 2) + 32 + (ks & 3) * 8,
-               sdesc_mnmajor<128, 128>(qb, ks), idTN, (it > 0 || ks > 0));
+        for (int u = 0; u < 4; ++u) {
+          const int ks = 4 * (u >> 1) + 2 * c + (u & 1);
+          mma_ts(tmem + C::TM_DV, tmem + C::TM_S + 64 * (ks >> 2) + (ks & 3) * 8, sdesc_mnmajor<128, 128>(db, ks),
+                 idTN, (it > 0 || ks > 0));
+        }
+      }
+      if (!ok) break;
+      // dK += dS^T Q_i (dS^T of block ks in columns 64 (ks/4) + 32 + 8 (ks%4))
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (!(ok = mbar_wait(bar(C::B_DSREADY + c), it & 1, guard, SITE_MMA))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ks = 4 * (u >> 1) + 2 * c + (u & 1);
+          mma_ts(tmem + C::TM_DK, tmem + C::TM_S + 64 * (ks >> 2) + 32 + (ks & 3) * 8,
+                 sdesc_mnmajor<128, 128>(qb, ks), idTN, (it > 0 || ks > 0));
+        }
+      }
+      if (!ok) break;
       mma_commit(bar(C::B_DKDONE));
       mma_commit(bar(C::B_QEMPTY + s));  // Q_i, dO_i have no later reader
       // dQ_i^T = K^T dS^T over the dP^T columns (the element-wise warps have read dP^T)
@@ -297,22 +313,23 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       const float4* D4 = L4 + C::BM / 4;
       const bool masked = (CAUSAL && kt * C::BN + C::BN - 1 > qh) || (kt * C::BN + C::BN > N);
       const uint64_t cc = f2pack(c_log2, c_log2);
-      // ---- P^T = 2^(S^T c - L log2 e), two columns per packed FMA
+      // ---- P^T = 2^(S^T c - L log2 e), two sub-chunks of 32 queries, each released
+      // to the dV product as soon as it is in tensor memory
       uint32_t pk[32];
-      {
-        uint32_t r[64];
-        tmem_ld32(tl + C::TM_S + 64 * h, r);
-        tmem_ld32(tl + C::TM_S + 64 * h + 32, r + 32);
-        tmem_ld_wait<64>(r);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::TM_S + 64 * h + 32 * c, r);
+        tmem_ld_wait<32>(r);
         auto body = [&](auto mask_tag) {
           constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            const float4 l = L4[v];
+          for (int v = 0; v < 8; ++v) {
+            const float4 l = L4[8 * c + v];
             float p[4];
 #pragma unroll
             for (int y = 0; y < 4; y += 2) {
-              const int x = 4 * v + y;
+              const int x = 4 * v + y;  // within the sub-chunk
               const uint64_t t = ffma2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), cc,
                                        y == 0 ? f2pack(l.x, l.y) : f2pack(l.z, l.w));
               float t0, t1;
@@ -320,36 +337,37 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
               p[y] = ex2(t0);
               p[y + 1] = ex2(t1);
               if (MASK) {
-                if ((CAUSAL && key > qh + x) || key >= N) p[y] = 0.f;
-                if ((CAUSAL && key > qh + x + 1) || key >= N) p[y + 1] = 0.f;
+                const int qx = qh + 32 * c + x;
+                if ((CAUSAL && key > qx) || key >= N) p[y] = 0.f;
+                if ((CAUSAL && key > qx + 1) || key >= N) p[y + 1] = 0.f;
               }
             }
-            pk[2 * v] = pack_bf16x2(p[0], p[1]);
-            pk[2 * v + 1] = pack_bf16x2(p[2], p[3]);
+            pk[16 * c + 2 * v] = pack_bf16x2(p[0], p[1]);
+            pk[16 * c + 2 * v + 1] = pack_bf16x2(p[2], p[3]);
           }
         };
         if (masked) body(std::true_type{}); else body(std::false_type{});
+        tmem_st16(tl + C::TM_S + 64 * h + 16 * c, pk + 16 * c);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PREADY + c));
       }
-      tmem_st32(tl + C::TM_S + 64 * h, pk);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_PREADY));
-      // ---- dS^T = P^T (dP^T - D), from the same bf16 P that enters dV
+      // ---- dS^T = P^T (dP^T - D), from the same bf16 P that enters dV; two sub-chunks
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), it & 1, guard, SITE_COMPUTE))) break;
       tc_fence_after();
-      uint32_t dk[32];
-      {
-        uint32_t r[64];
-        tmem_ld32(tl + C::TM_DP + 64 * h, r);
-        tmem_ld32(tl + C::TM_DP + 64 * h + 32, r + 32);
-        tmem_ld_wait<64>(r);
+      uint8_t* row = tiles + C::T_DS + h * (128 * 128) + kr * 128;
 #pragma unroll
-        for (int v = 0; v < 16; ++v) {
-          const float4 dd = D4[v];
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32], dk[16];
+        tmem_ld32(tl + C::TM_DP + 64 * h + 32 * c, r);
+        tmem_ld_wait<32>(r);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 dd = D4[8 * c + v];
 #pragma unroll
           for (int y = 0; y < 4; y += 2) {
             const int x = 4 * v + y;
-            const uint32_t w = pk[x >> 1];
+            const uint32_t w = pk[16 * c + (x >> 1)];
             const uint64_t pp = f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
             const uint64_t t = fadd2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])),
                                      y == 0 ? f2pack(-dd.x, -dd.y) : f2pack(-dd.z, -dd.w));
@@ -358,18 +376,18 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
             dk[x >> 1] = pack_bf16x2(d0, d1);
           }
         }
-      }
-      tmem_st32(tl + C::TM_S + 64 * h + 32, dk);
-      // dS^T row kr, queries 64h .. 64h+63: one 128-byte swizzled row of chunk h
-      uint8_t* row = tiles + C::T_DS + h * (128 * 128) + kr * 128;
+        tmem_st16(tl + C::TM_S + 64 * h + 32 + 16 * c, dk);
+        // dS^T row kr, queries 64h + 32c .. +31: four 16-byte units of the swizzled row
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(row + ((u ^ (kr & 7)) << 4)) =
-            make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_DSREADY));
+        for (int u = 0; u < 4; ++u)
+          *reinterpret_cast<uint4*>(row + (((4 * c + u) ^ (kr & 7)) << 4)) =
+              make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DSREADY + c));
+      }
+
     }
     // dK (times scale) and dV: this warp's lane quarter, d columns 64h .. 64h+63
     if (ok) ok = mbar_wait_warp(bar(C::B_FINAL), 0, guard, SITE_COMPUTE);
