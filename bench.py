@@ -240,6 +240,7 @@ def run_ours(args):
 
     w = si.WORKLOADS[args.workload]
     causal = True if len(w.causal) == 1 and w.causal[0] else (args.causal if args.causal is not None else w.causal[-1])
+    fa.check(fa.fa_debug_set_bwd_split(args.bwd_split), "fa_debug_set_bwd_split")
     r = Runner(fa, torch, w, causal, dev)
     flops_f, flops_b = w.fwd_flops(causal), w.bwd_flops(causal)
 
@@ -371,6 +372,8 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(si.WORKLOADS))
     ap.add_argument("--causal", type=int, default=None, help="for workloads that run both mask modes")
     ap.add_argument("--quick", action="store_true", help="headline timing only (for profiler runs)")
+    ap.add_argument("--bwd-split", type=int, default=0, choices=[0, 1, 2],
+                    help="backward form for d=128: 1 one kernel + dQ reduction, 2 two kernels, 0 library default")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.quick:
         ap.error("at least 3 warm-up steps")

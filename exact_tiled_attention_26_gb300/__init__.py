@@ -19,7 +19,7 @@ __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_WORKSPACE",
     "FAError", "lib", "lib_path", "fa_fwd", "fa_bwd_preprocess", "fa_bwd_workspace_size", "fa_bwd",
     "fa_bwd_noalloc", "FA_NOALLOC_MAX_WORKSPACE_BYTES",
-    "fa_status_string", "fa_get_tile_config", "fa_tile_pairs", "fa_debug_set_tile_counter",
+    "fa_status_string", "fa_get_tile_config", "fa_tile_pairs", "fa_debug_set_tile_counter", "fa_debug_set_bwd_split",
     "fa_poll_device_error", "fa_debug_timeout_probe", "fa_selftest_umma", "fa_version",
     "attention_forward", "attention_backward", "check",
 ]
@@ -57,6 +57,7 @@ _sig = {
     "fa_get_tile_config": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fa_tile_pairs": (ctypes.c_longlong, [_i, _i, _i, _i]),
     "fa_debug_set_tile_counter": (_i, [_vp]),
+    "fa_debug_set_bwd_split": (_i, [_i]),
     "fa_poll_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
     "fa_debug_timeout_probe": (_i, [_i, _vp]),
     "fa_selftest_umma": (_i, [_i, _vp, _vp, _vp, _i, _i, _vp]),
@@ -111,6 +112,10 @@ def fa_tile_pairs(N, d, causal, pass_):
 
 def fa_debug_set_tile_counter(dev_counter):
     return lib.fa_debug_set_tile_counter(dev_counter)
+
+
+def fa_debug_set_bwd_split(split):
+    return lib.fa_debug_set_bwd_split(split)
 
 
 def fa_poll_device_error(stream):

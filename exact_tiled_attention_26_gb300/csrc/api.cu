@@ -19,6 +19,8 @@ constexpr int kMaxDevices = 64;
 int* g_status_ptr[kMaxDevices] = {nullptr};
 std::mutex g_mu;
 unsigned long long* g_tile_counter = nullptr;
+int g_bwd_split = 0;                    // 0: the default below
+constexpr int kDefaultBwdSplitD128 = 1;  // chosen by measurement on GB300
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -193,12 +195,25 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int 
   return launch_preprocess(O, dO, D, static_cast<long long>(B) * H * N, d, stream);
 }
 
+// Which backward form runs: 1 = one kernel over key tiles with dQ reduced in
+// the fp32 workspace, 2 = two kernels (key tiles for dK, dV; query tiles for dQ).
+static int bwd_split(int d) {
+  if (d != 128) return 1;
+  return g_bwd_split != 0 ? g_bwd_split : kDefaultBwdSplitD128;
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
   (void)causal;
   bool empty = false;
   if (check_shape(B, H, N, d, &empty) != FA_OK) return static_cast<size_t>(-1);
-  if (empty) return 0;
+  if (empty || bwd_split(d) == 2) return 0;
   return static_cast<size_t>(B) * H * N * d * sizeof(float);
+}
+
+fa_status fa_debug_set_bwd_split(int split) {
+  if (split < 0 || split > 2) return FA_ERR_INVALID_ARG;
+  g_bwd_split = split;
+  return FA_OK;
 }
 
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
@@ -215,12 +230,14 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
       !aligned(dK, 16) || !aligned(dV, 16) || !aligned(L, 4) || !aligned(D, 4))
     return FA_ERR_INVALID_ARG;
   const size_t need = fa_bwd_workspace_size(B, H, N, d, causal);
-  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return FA_ERR_WORKSPACE;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
+    return FA_ERR_WORKSPACE;
   int* status = device_status_word();
   if (status == nullptr) return FA_ERR_CUDA;
-  if (cudaMemsetAsync(workspace, 0, need, stream) != cudaSuccess) return FA_ERR_CUDA;
   BwdLaunch a{Q, K, V, dO, L, D, static_cast<float*>(workspace), dK, dV, B * H, N, d, causal ? 1 : 0, scale,
               stream, status, g_tile_counter};
+  if (bwd_split(d) == 2) return launch_bwd_two_kernel_d128(a, dQ);
+  if (cudaMemsetAsync(workspace, 0, need, stream) != cudaSuccess) return FA_ERR_CUDA;
   st = launch_bwd(a);
   if (st != FA_OK) return st;
   return launch_dq_convert(static_cast<const float*>(workspace), dQ, static_cast<long long>(B) * H * N * d, scale,

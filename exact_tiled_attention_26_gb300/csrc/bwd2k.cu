@@ -1,0 +1,607 @@
+// Backward pass, head size 128: the two-kernel form of "CS336 Assignment 2
+// notes" §1.4 (kernel 1 iterates key/value tiles in its outer loop and forms
+// dK, dV; kernel 2 iterates query tiles and forms dQ; S and P are computed in
+// both).  No atomics and no workspace: each output is written once.
+//
+// bwd_kv_kernel: one CTA per 128 keys (keys on the 128 tensor-memory lanes),
+//   S^T = K Q_i^T, dP^T = V dO_i^T (UMMA), P^T, dS^T (8 element-wise warps, in two
+//   32-query sub-chunks), dV += P^T dO_i, dK += dS^T Q_i (UMMA, A from tensor
+//   memory).  Tensor memory: dK | dV | two regions that take turns holding S^T
+//   (then P^T | dS^T) and dP^T.
+// bwd_q_kernel: one CTA per 128 queries (queries on the lanes; L and D of the
+//   row kept in registers), S = Q K_j^T (two buffers), dP = dO V_j^T (UMMA),
+//   P = 2^(S c - L log2 e), dS = P (dP - D) (8 warps, two per lane quarter, one
+//   per 64-key half), dQ += dS K_j (UMMA, A = dS in tensor memory), then
+//   dQ * scale -> bf16.  Tensor memory: S x2 | dP | dQ.
+// Both kernels split UMMA issue over two threads, as the other kernels do.
+#include <type_traits>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int TILE = 128 * 128 * 2;  // one 128 x 128 bf16 tile (two 64-column chunks)
+constexpr int SMEM_MAX = 232448;
+
+enum : int { SITE_KV = 0x221, SITE_Q = 0x222 };
+
+// ============================================================================ dK, dV
+struct KVC {
+  static constexpr int NTHREADS = 384, NCOMP = 256;
+  enum : int {
+    B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6,
+    B_PREADY = 7,  // [step parity][sub-chunk]: the element-wise warps may be a step ahead of issuer B
+    B_DSREADY = 11, B_DKDONE = 13, B_DPCONS = 14, B_FINAL = 15, B_ADONE = 16, NBAR = 17
+  };
+  static constexpr int OFF_MISC = NBAR * 8, OFF_LD = 256, LD_BYTES = 2 * 128 * 4;
+  static constexpr int SMALL = OFF_LD + 2 * LD_BYTES;
+  static constexpr int T_K = 0, T_V = TILE, T_Q = 2 * TILE, T_DO = 3 * TILE;  // Q, dO: + s * 2 TILE
+  static constexpr int TILES = 6 * TILE;
+  static constexpr int SMEM = SMALL + 1024 + TILES;
+  // Two 128-column regions alternate: step i keeps S^T (then P^T | dS^T) in region
+  // i % 2 and dP^T in region (i + 1) % 2, so S^T of step i+1 can be formed as soon
+  // as dP^T of step i has been read, while dK of step i is still being accumulated.
+  static constexpr int TM_DK = 0, TM_DV = 128, TM_R = 256;
+};
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(KVC::NTHREADS, 1)
+    bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                  const float* __restrict__ Lg, const float* __restrict__ Dg, __nv_bfloat16* __restrict__ dK,
+                  __nv_bfloat16* __restrict__ dV, int N, float c_log2, float scale, int* status,
+                  unsigned long long* tile_counter) {
+  using C = KVC;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* tiles = align1024(smem_raw + C::SMALL);
+  const uint32_t sb = smem_u32(smem_raw), tb = smem_u32(tiles);
+  auto bar = [&](int i) -> uint32_t { return sb + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + C::OFF_MISC + 4);
+  const Guard guard{status, abort_flag};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kt = blockIdx.x, bh = blockIdx.y;
+  const int Tq = (N + 127) / 128;
+  const int i0 = CAUSAL ? kt : 0;
+  const int n_it = Tq - i0;
+  const size_t row0 = static_cast<size_t>(bh) * N;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_KV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(C::B_QFULL + s), 1 + 32);
+      mbar_init(bar(C::B_QEMPTY + s), 1);
+      mbar_init(bar(C::B_PREADY + 2 * s), C::NCOMP);
+      mbar_init(bar(C::B_PREADY + 2 * s + 1), C::NCOMP);
+      mbar_init(bar(C::B_DSREADY + s), C::NCOMP);
+    }
+    mbar_init(bar(C::B_SFULL), 1);
+    mbar_init(bar(C::B_DPFULL), 1);
+    mbar_init(bar(C::B_DKDONE), 1);
+    mbar_init(bar(C::B_DPCONS), C::NCOMP);
+    mbar_init(bar(C::B_FINAL), 1);
+    mbar_init(bar(C::B_ADONE), 1);
+    *abort_flag = (*reinterpret_cast<volatile int*>(status) != 0);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool skip = *abort_flag != 0;
+
+  if (warp == 0 && !skip) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      mbar_expect_tx(bar(C::B_KV), 2 * TILE);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_3d(tb + C::T_K + c * 128 * 128, &tmK, bar(C::B_KV), c * 64, kt * 128, bh);
+        tma_load_3d(tb + C::T_V + c * 128 * 128, &tmV, bar(C::B_KV), c * 64, kt * 128, bh);
+      }
+    }
+    int last = -1;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1, q0 = (i0 + it) * 128;
+      float lv[4], dv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q0 + lane + 32 * u;
+        lv[u] = q < N ? -Lg[row0 + q] * kLog2e : -INFINITY;
+        dv[u] = q < N ? Dg[row0 + q] : 0.f;
+      }
+      if (!mbar_wait_warp(bar(C::B_QEMPTY + s), ((it >> 1) & 1) ^ 1, guard, SITE_KV)) break;
+      if (lane == 0) {
+        mbar_expect_tx(bar(C::B_QFULL + s), 2 * TILE);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(tb + C::T_Q + s * 2 * TILE + c * 128 * 128, &tmQ, bar(C::B_QFULL + s), c * 64, q0, bh);
+          tma_load_3d(tb + C::T_DO + s * 2 * TILE + c * 128 * 128, &tmdO, bar(C::B_QFULL + s), c * 64, q0, bh);
+        }
+      }
+      float* Ls = reinterpret_cast<float*>(smem_raw + C::OFF_LD + s * C::LD_BYTES);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        Ls[lane + 32 * u] = lv[u];
+        Ls[128 + lane + 32 * u] = dv[u];
+      }
+      mbar_arrive(bar(C::B_QFULL + s));
+      last = it;
+    }
+    if (lane == 0 && *abort_flag) {
+      mbar_drain(bar(C::B_KV), 0);
+      for (int it = (last > 0 ? last - 1 : 0); it <= last; ++it) mbar_drain(bar(C::B_QFULL + (it & 1)), (it >> 1) & 1);
+    }
+  } else if (warp == 1 && lane == 0 && !skip) {
+    // ---------------------------------------------------------------- issuer A: S^T, dP^T
+    constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);
+    const uint32_t kb = tb + C::T_K, vb = tb + C::T_V;
+    bool ok = mbar_wait(bar(C::B_KV), 0, guard, SITE_KV);
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int s = it & 1;
+      const uint32_t qb = tb + C::T_Q + s * 2 * TILE, db = tb + C::T_DO + s * 2 * TILE;
+      const uint32_t rs = tmem + C::TM_R + 128 * s, rd = tmem + C::TM_R + 128 * (s ^ 1);
+      if (!(ok = mbar_wait(bar(C::B_QFULL + s), (it >> 1) & 1, guard, SITE_KV))) break;
+      // region s held dP^T of the last step: every element-wise thread has read it
+      if (it > 0 && !(ok = mbar_wait(bar(C::B_DPCONS), (it - 1) & 1, guard, SITE_KV))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(rs, sdesc_kmajor<128, 128>(kb, ks), sdesc_kmajor<128, 128>(qb, ks), idKK, ks > 0);
+      mma_commit(bar(C::B_SFULL));
+      // region s^1 held P^T and dS^T of the last step until dV and dK read them
+      if (it > 0 && !(ok = mbar_wait(bar(C::B_DKDONE), (it - 1) & 1, guard, SITE_KV))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(rd, sdesc_kmajor<128, 128>(vb, ks), sdesc_kmajor<128, 128>(db, ks), idKK, ks > 0);
+      mma_commit(bar(C::B_DPFULL));
+    }
+    mma_commit(bar(C::B_ADONE));
+    if (ok && tile_counter != nullptr) atomicAdd(tile_counter, static_cast<unsigned long long>(n_it));
+  } else if (warp == 2 && lane == 0 && !skip) {
+    // ---------------------------------------------------------------- issuer B: dV, dK
+    constexpr uint32_t idTN = idesc_bf16(128, 128, false, true);
+    bool ok = true;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int s = it & 1;
+      const uint32_t qb = tb + C::T_Q + s * 2 * TILE, db = tb + C::T_DO + s * 2 * TILE;
+      const uint32_t rs = tmem + C::TM_R + 128 * s;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (!(ok = mbar_wait(bar(C::B_PREADY + 2 * s + c), (it >> 1) & 1, guard, SITE_KV))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ks = 4 * (u >> 1) + 2 * c + (u & 1);
+          mma_ts(tmem + C::TM_DV, rs + 64 * (ks >> 2) + (ks & 3) * 8, sdesc_mnmajor<128, 128>(db, ks), idTN,
+                 (it > 0 || ks > 0));
+        }
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (!(ok = mbar_wait(bar(C::B_DSREADY + c), it & 1, guard, SITE_KV))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ks = 4 * (u >> 1) + 2 * c + (u & 1);
+          mma_ts(tmem + C::TM_DK, rs + 64 * (ks >> 2) + 32 + (ks & 3) * 8, sdesc_mnmajor<128, 128>(qb, ks), idTN,
+                 (it > 0 || ks > 0));
+        }
+      }
+      if (!ok) break;
+      mma_commit(bar(C::B_DKDONE));
+      mma_commit(bar(C::B_QEMPTY + s));
+    }
+    mma_commit(bar(C::B_FINAL));
+  } else if (warp >= 4 && !skip) {
+    // ---------------------------------------------------------------- element-wise warps
+    const int qw = warp & 3, h = (warp - 4) >> 2, kr = qw * 32 + lane, key = kt * 128 + kr;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    const uint64_t cc = f2pack(c_log2, c_log2);
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it & 1;
+      if (!(ok = mbar_wait_warp(bar(C::B_QFULL + s), (it >> 1) & 1, guard, SITE_KV))) break;
+      if (!(ok = mbar_wait_warp(bar(C::B_SFULL), it & 1, guard, SITE_KV))) break;
+      tc_fence_after();
+      const uint32_t rs = tl + C::TM_R + 128 * s, rd = tl + C::TM_R + 128 * (s ^ 1);
+      const int qh = (i0 + it) * 128 + 64 * h;
+      const float4* L4 = reinterpret_cast<const float4*>(smem_raw + C::OFF_LD + s * C::LD_BYTES) + 16 * h;
+      const float4* D4 = L4 + 32;
+      const bool masked = (CAUSAL && kt * 128 + 127 > qh) || (kt * 128 + 128 > N);
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(rs + 64 * h + 32 * c, r);
+        tmem_ld_wait<32>(r);
+        auto body = [&](auto mask_tag) {
+          constexpr bool MASK = decltype(mask_tag)::value;
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            const float4 l = L4[8 * c + v];
+            float p[4];
+#pragma unroll
+            for (int y = 0; y < 4; y += 2) {
+              const int x = 4 * v + y;
+              float t0, t1;
+              f2unpack(ffma2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), cc,
+                             y == 0 ? f2pack(l.x, l.y) : f2pack(l.z, l.w)),
+                       t0, t1);
+              p[y] = ex2(t0);
+              p[y + 1] = ex2(t1);
+              if (MASK) {
+                const int qx = qh + 32 * c + x;
+                if ((CAUSAL && key > qx) || key >= N) p[y] = 0.f;
+                if ((CAUSAL && key > qx + 1) || key >= N) p[y + 1] = 0.f;
+              }
+            }
+            pk[16 * c + 2 * v] = pack_bf16x2(p[0], p[1]);
+            pk[16 * c + 2 * v + 1] = pack_bf16x2(p[2], p[3]);
+          }
+        };
+        if (masked) body(std::true_type{}); else body(std::false_type{});
+        tmem_st16(rs + 64 * h + 16 * c, pk + 16 * c);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_PREADY + 2 * s + c));
+      }
+      if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), it & 1, guard, SITE_KV))) break;
+      tc_fence_after();
+      // take all of this thread's dP^T out of tensor memory first, so that S^T of the
+      // next step can be formed in its region while dS is computed
+      uint32_t rdp[64];
+      tmem_ld32(rd + 64 * h, rdp);
+      tmem_ld32(rd + 64 * h + 32, rdp + 32);
+      tmem_ld_wait<64>(rdp);
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DPCONS));
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t* r = rdp + 32 * c;
+        uint32_t dk[16];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 dd = D4[8 * c + v];
+#pragma unroll
+          for (int y = 0; y < 4; y += 2) {
+            const int x = 4 * v + y;
+            const uint32_t w = pk[16 * c + (x >> 1)];
+            float d0, d1;
+            f2unpack(fmul2(f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
+                           fadd2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])),
+                                 y == 0 ? f2pack(-dd.x, -dd.y) : f2pack(-dd.z, -dd.w))),
+                     d0, d1);
+            dk[x >> 1] = pack_bf16x2(d0, d1);
+          }
+        }
+        tmem_st16(rs + 64 * h + 32 + 16 * c, dk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DSREADY + c));
+      }
+    }
+    if (ok) ok = mbar_wait_warp(bar(C::B_FINAL), 0, guard, SITE_KV);
+    if (ok) {
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const float f = t == 0 ? scale : 1.f;
+        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (row0 + key) * 128 + 64 * h;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 64 * h + 32 * c, r);
+          tmem_ld_wait<32>(r);
+          if (key < N) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * f, __uint_as_float(r[8 * i + 1]) * f),
+                                 pack_bf16x2(__uint_as_float(r[8 * i + 2]) * f, __uint_as_float(r[8 * i + 3]) * f),
+                                 pack_bf16x2(__uint_as_float(r[8 * i + 4]) * f, __uint_as_float(r[8 * i + 5]) * f),
+                                 pack_bf16x2(__uint_as_float(r[8 * i + 6]) * f, __uint_as_float(r[8 * i + 7]) * f));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (!skip && *abort_flag) {
+      if (lane == 0) {
+        mbar_drain(bar(C::B_ADONE), 0);
+        mbar_drain(bar(C::B_FINAL), 0);
+      }
+      __syncwarp();
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================================ dQ
+struct QC {
+  static constexpr int NTHREADS = 384, NCOMP = 256;
+  // K_j lives until dQ_j is done, V_j only until dP_j is: three K stages and two
+  // V stages let each load start two steps ahead of its use.
+  static constexpr int KST = 3, VST = 2;
+  enum : int {
+    B_QDO = 0, B_KFULL = 1, B_KEMPTY = 4, B_VFULL = 7, B_VEMPTY = 9, B_SFULL = 11, B_SFREE = 13, B_DPFULL = 15,
+    B_DSREADY = 16,  // [S buffer][sub-chunk]
+    B_FINAL = 20, B_ADONE = 21, B_DPCONS = 22, NBAR = 23
+  };
+  static constexpr int OFF_MISC = NBAR * 8;
+  static constexpr int SMALL = 256;
+  static constexpr int T_Q = 0, T_DO = TILE, T_K = 2 * TILE, T_V = (2 + KST) * TILE;  // stage k: + k TILE
+  static constexpr int TILES = (2 + KST + VST) * TILE;
+  static constexpr int SMEM = SMALL + 1024 + TILES;
+  static constexpr int TM_S = 0, TM_DP = 256, TM_DQ = 384;  // S buffer b at TM_S + 128 b
+};
+
+template <bool CAUSAL>
+__global__ void __launch_bounds__(QC::NTHREADS, 1)
+    bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                 const float* __restrict__ Lg, const float* __restrict__ Dg, __nv_bfloat16* __restrict__ dQ, int N,
+                 float c_log2, float scale, int* status) {
+  using C = QC;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* tiles = align1024(smem_raw + C::SMALL);
+  const uint32_t sb = smem_u32(smem_raw), tb = smem_u32(tiles);
+  auto bar = [&](int i) -> uint32_t { return sb + 8 * i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + C::OFF_MISC + 4);
+  const Guard guard{status, abort_flag};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = (N + 127) / 128;
+  const int qt = T - 1 - static_cast<int>(blockIdx.x);  // longest causal rows first
+  const int bh = blockIdx.y;
+  const int n_kv = CAUSAL ? min(T, (min((qt + 1) * 128, N) - 1) / 128 + 1) : T;
+  const size_t row0 = static_cast<size_t>(bh) * N;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(C::B_QDO), 1);
+    for (int k = 0; k < C::KST; ++k) {
+      mbar_init(bar(C::B_KFULL + k), 1);
+      mbar_init(bar(C::B_KEMPTY + k), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::B_VFULL + b), 1);
+      mbar_init(bar(C::B_VEMPTY + b), 1);
+      mbar_init(bar(C::B_SFULL + b), 1);
+      mbar_init(bar(C::B_SFREE + b), 1);
+      for (int c = 0; c < 2; ++c) mbar_init(bar(C::B_DSREADY + 2 * b + c), C::NCOMP);
+    }
+    mbar_init(bar(C::B_DPFULL), 1);
+    mbar_init(bar(C::B_DPCONS), C::NCOMP);
+    mbar_init(bar(C::B_FINAL), 1);
+    mbar_init(bar(C::B_ADONE), 1);
+    *abort_flag = (*reinterpret_cast<volatile int*>(status) != 0);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const bool skip = *abort_flag != 0;
+
+  if (warp == 0 && lane == 0 && !skip) {
+    // ---------------------------------------------------------------- producer
+    mbar_expect_tx(bar(C::B_QDO), 2 * TILE);
+    for (int c = 0; c < 2; ++c) {
+      tma_load_3d(tb + C::T_Q + c * 128 * 128, &tmQ, bar(C::B_QDO), c * 64, qt * 128, bh);
+      tma_load_3d(tb + C::T_DO + c * 128 * 128, &tmdO, bar(C::B_QDO), c * 64, qt * 128, bh);
+    }
+    int lastk = -1, lastv = -1;
+    for (int j = 0; j < n_kv; ++j) {
+      const int k = j % C::KST, v = j & 1;
+      if (!mbar_wait(bar(C::B_KEMPTY + k), ((j / C::KST) & 1) ^ 1, guard, SITE_Q)) break;
+      mbar_expect_tx(bar(C::B_KFULL + k), TILE);
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d(tb + C::T_K + k * TILE + c * 128 * 128, &tmK, bar(C::B_KFULL + k), c * 64, j * 128, bh);
+      lastk = j;
+      if (!mbar_wait(bar(C::B_VEMPTY + v), ((j >> 1) & 1) ^ 1, guard, SITE_Q)) break;
+      mbar_expect_tx(bar(C::B_VFULL + v), TILE);
+      for (int c = 0; c < 2; ++c)
+        tma_load_3d(tb + C::T_V + v * TILE + c * 128 * 128, &tmV, bar(C::B_VFULL + v), c * 64, j * 128, bh);
+      lastv = j;
+    }
+    if (*abort_flag) {
+      mbar_drain(bar(C::B_QDO), 0);
+      for (int j = max(lastk - (C::KST - 1), 0); j <= lastk; ++j)
+        mbar_drain(bar(C::B_KFULL + j % C::KST), (j / C::KST) & 1);
+      for (int j = max(lastv - 1, 0); j <= lastv; ++j) mbar_drain(bar(C::B_VFULL + (j & 1)), (j >> 1) & 1);
+    }
+  } else if (warp == 1 && lane == 0 && !skip) {
+    // ---------------------------------------------------------------- issuer A: S, dP
+    constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);
+    const uint32_t qb = tb + C::T_Q, db = tb + C::T_DO;
+    bool ok = mbar_wait(bar(C::B_QDO), 0, guard, SITE_Q);
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j & 1, k = j % C::KST;
+      const uint32_t kb = tb + C::T_K + k * TILE, vb = tb + C::T_V + s * TILE;
+      if (!(ok = mbar_wait(bar(C::B_KFULL + k), (j / C::KST) & 1, guard, SITE_Q))) break;
+      // S buffer s last held dS_{j-2}: dQ_{j-2} must have read it
+      if (j >= 2 && !(ok = mbar_wait(bar(C::B_SFREE + s), ((j >> 1) & 1) ^ 1, guard, SITE_Q))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tmem + C::TM_S + 128 * s, sdesc_kmajor<128, 128>(qb, ks), sdesc_kmajor<128, 128>(kb, ks), idKK, ks > 0);
+      mma_commit(bar(C::B_SFULL + s));
+      // the dP columns are free once every element-wise thread has read dP_{j-1}
+      if (j > 0 && !(ok = mbar_wait(bar(C::B_DPCONS), (j - 1) & 1, guard, SITE_Q))) break;
+      if (!(ok = mbar_wait(bar(C::B_VFULL + s), (j >> 1) & 1, guard, SITE_Q))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tmem + C::TM_DP, sdesc_kmajor<128, 128>(db, ks), sdesc_kmajor<128, 128>(vb, ks), idKK, ks > 0);
+      mma_commit(bar(C::B_DPFULL));
+      mma_commit(bar(C::B_VEMPTY + s));
+    }
+    mma_commit(bar(C::B_ADONE));
+  } else if (warp == 2 && lane == 0 && !skip) {
+    // ---------------------------------------------------------------- issuer B: dQ
+    constexpr uint32_t idTN = idesc_bf16(128, 128, false, true);  // dS (tensor memory) x K (N-major)
+    bool ok = true;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int s = j & 1, k = j % C::KST;
+      const uint32_t kb = tb + C::T_K + k * TILE;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        if (!(ok = mbar_wait(bar(C::B_DSREADY + 2 * s + c), (j >> 1) & 1, guard, SITE_Q))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int ks = 4 * (u >> 1) + 2 * c + (u & 1);  // key block: half ks/4, sub-chunk (ks%4)/2
+          mma_ts(tmem + C::TM_DQ, tmem + C::TM_S + 128 * s + 64 * (ks >> 2) + (ks & 3) * 8,
+                 sdesc_mnmajor<128, 128>(kb, ks), idTN, (j > 0 || ks > 0));
+        }
+      }
+      if (!ok) break;
+      mma_commit(bar(C::B_SFREE + s));
+      mma_commit(bar(C::B_KEMPTY + k));  // S_j completed before dS_j existed
+    }
+    mma_commit(bar(C::B_FINAL));
+  } else if (warp >= 4 && !skip) {
+    // ---------------------------------------------------------------- element-wise warps
+    const int qw = warp & 3, h = (warp - 4) >> 2, row = qw * 32 + lane, q = qt * 128 + row;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
+    const float nl = q < N ? -Lg[row0 + q] * kLog2e : -INFINITY;  // rows past N: P = 0
+    const float dq = q < N ? Dg[row0 + q] : 0.f;
+    const uint64_t cc = f2pack(c_log2, c_log2), nl2 = f2pack(nl, nl), nd2 = f2pack(-dq, -dq);
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      const int s = j & 1;
+      if (!(ok = mbar_wait_warp(bar(C::B_SFULL + s), (j >> 1) & 1, guard, SITE_Q))) break;
+      tc_fence_after();
+      const int kh = j * 128 + 64 * h;  // first key of this half
+      const bool masked = (CAUSAL && kh + 63 > qt * 128) || (kh + 64 > N);
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::TM_S + 128 * s + 64 * h + 32 * c, r);
+        tmem_ld_wait<32>(r);
+        auto body = [&](auto mask_tag) {
+          constexpr bool MASK = decltype(mask_tag)::value;
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            float t0, t1;
+            f2unpack(ffma2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), cc, nl2), t0, t1);
+            float p0 = ex2(t0), p1 = ex2(t1);
+            if (MASK) {
+              const int k = kh + 32 * c + x;
+              if ((CAUSAL && k > q) || k >= N) p0 = 0.f;
+              if ((CAUSAL && k + 1 > q) || k + 1 >= N) p1 = 0.f;
+            }
+            pk[16 * c + (x >> 1)] = pack_bf16x2(p0, p1);
+          }
+        };
+        if (masked) body(std::true_type{}); else body(std::false_type{});
+      }
+      if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), j & 1, guard, SITE_Q))) break;
+      tc_fence_after();
+      uint32_t rdp[64];
+      tmem_ld32(tl + C::TM_DP + 64 * h, rdp);
+      tmem_ld32(tl + C::TM_DP + 64 * h + 32, rdp + 32);
+      tmem_ld_wait<64>(rdp);
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DPCONS));
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t* r = rdp + 32 * c;
+        uint32_t dk[16];
+#pragma unroll
+        for (int x = 0; x < 32; x += 2) {
+          const uint32_t w = pk[16 * c + (x >> 1)];
+          float d0, d1;
+          f2unpack(fmul2(f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
+                         fadd2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), nd2)),
+                   d0, d1);
+          dk[x >> 1] = pack_bf16x2(d0, d1);
+        }
+        // dS of keys kh + 32c .. +31 over S columns this half has already read
+        tmem_st16(tl + C::TM_S + 128 * s + 64 * h + 16 * c, dk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::B_DSREADY + 2 * s + c));
+      }
+    }
+    if (ok) ok = mbar_wait_warp(bar(C::B_FINAL), 0, guard, SITE_Q);
+    if (ok) {
+      tc_fence_after();
+      __nv_bfloat16* dst = dQ + (row0 + q) * 128 + 64 * h;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tl + C::TM_DQ + 64 * h + 32 * c, r);
+        tmem_ld_wait<32>(r);
+        if (q < N) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * scale, __uint_as_float(r[8 * i + 1]) * scale),
+                               pack_bf16x2(__uint_as_float(r[8 * i + 2]) * scale, __uint_as_float(r[8 * i + 3]) * scale),
+                               pack_bf16x2(__uint_as_float(r[8 * i + 4]) * scale, __uint_as_float(r[8 * i + 5]) * scale),
+                               pack_bf16x2(__uint_as_float(r[8 * i + 6]) * scale, __uint_as_float(r[8 * i + 7]) * scale));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (!skip && *abort_flag) {
+      if (lane == 0) {
+        mbar_drain(bar(C::B_ADONE), 0);
+        mbar_drain(bar(C::B_FINAL), 0);
+      }
+      __syncwarp();
+    }
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool CAUSAL>
+fa_status launch_t(const BwdLaunch& a, void* dQ) {
+  CUtensorMap mQ, mK, mV, mdO;
+  if (!encode_bf16_3d(&mQ, a.Q, 128, a.N, a.BH, 64, 128) || !encode_bf16_3d(&mdO, a.dO, 128, a.N, a.BH, 64, 128) ||
+      !encode_bf16_3d(&mK, a.K, 128, a.N, a.BH, 64, 128) || !encode_bf16_3d(&mV, a.V, 128, a.N, a.BH, 64, 128))
+    return FA_ERR_CUDA;
+  static_assert(KVC::SMEM <= SMEM_MAX && QC::SMEM <= SMEM_MAX, "shared memory budget");
+  auto kkv = bwd_kv_kernel<CAUSAL>;
+  auto kq = bwd_q_kernel<CAUSAL>;
+  if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, KVC::SMEM) != cudaSuccess ||
+      cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, QC::SMEM) != cudaSuccess)
+    return FA_ERR_CUDA;
+  const int T = (a.N + 127) / 128;
+  const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  kkv<<<dim3(T, a.BH), KVC::NTHREADS, KVC::SMEM, a.stream>>>(
+      mQ, mK, mV, mdO, a.L, a.D, static_cast<__nv_bfloat16*>(a.dK), static_cast<__nv_bfloat16*>(a.dV), a.N, c_log2,
+      a.scale, a.status, a.counter);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  kq<<<dim3(T, a.BH), QC::NTHREADS, QC::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D,
+                                                          static_cast<__nv_bfloat16*>(dQ), a.N, c_log2, a.scale,
+                                                          a.status);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+fa_status launch_bwd_two_kernel_d128(const BwdLaunch& a, void* dQ) {
+  return a.causal ? launch_t<true>(a, dQ) : launch_t<false>(a, dQ);
+}
+
+}  // namespace fa

@@ -79,8 +79,10 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, float* D,
 
 /*
  * Bytes of device workspace fa_bwd needs: an fp32 [B,H,N,d] accumulator for
- * dQ (key tiles add their dS K contributions into it).  0 for empty inputs;
- * (size_t)-1 for invalid sizes.
+ * dQ (key tiles add their dS K contributions into it) when the one-kernel
+ * backward runs; 0 when the two-kernel backward runs (see
+ * fa_debug_set_bwd_split) or for empty inputs; (size_t)-1 for invalid sizes.
+ * Query it after any change of the backward split.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal);
 
@@ -157,6 +159,19 @@ long long fa_tile_pairs(int N, int d, int causal, int pass);
  * Process-wide setting.
  */
 fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter);
+
+/*
+ * Debug: which form of the backward fa_bwd runs for d = 128 ("CS336
+ * Assignment 2 notes" §1.4 leaves the split open):
+ *   1: one kernel, key/value tiles outer; dQ accumulated in the fp32 workspace
+ *      and rounded to bf16 by a second pass;
+ *   2: two kernels, key/value tiles outer for dK and dV, then query tiles outer
+ *      for dQ (S and P recomputed in both); no workspace, no reductions;
+ *   0: the library's default (the faster of the two on GB300).
+ * d = 32 and 64 always run form 1.  Process-wide setting; FA_ERR_INVALID_ARG
+ * for other values.
+ */
+fa_status fa_debug_set_bwd_split(int split);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

@@ -51,10 +51,13 @@ def lib():
     return fa
 
 
-def run_gpu(Q, K, V, dO, causal, scale=None, counter=False):
+def run_gpu(Q, K, V, dO, causal, scale=None, counter=False, split=0):
     """Forward + preprocess + backward through the C ABI.  Inputs: bf16 CPU tensors
-    [B,H,N,d].  Returns CPU tensors and (if asked) the tile-pair counts."""
+    [B,H,N,d].  `split` selects the backward form (fa_debug_set_bwd_split; 0 =
+    the library's default).  Returns CPU tensors and (if asked) the tile-pair
+    counts."""
     fa = lib()
+    fa.check(fa.fa_debug_set_bwd_split(split))
     B, H, N, d = Q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dev = torch.device("cuda")
@@ -79,6 +82,7 @@ def run_gpu(Q, K, V, dO, causal, scale=None, counter=False):
                            D.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, causal, scale,
                            ws.data_ptr(), ws.numel(), s), "fa_bwd")
     finally:
+        fa.fa_debug_set_bwd_split(0)
         if counter:
             fa.fa_debug_set_tile_counter(None)
     st, detail = fa.fa_poll_device_error(s)

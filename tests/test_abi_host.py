@@ -111,3 +111,19 @@ def test_tile_pair_counts_for_the_workloads(fa_lib):
         assert fa_lib.fa_tile_pairs(N, 128, True, 0) == pairs
         T = N // 128
         assert fa_lib.fa_tile_pairs(N, 128, False, 0) == T * T
+
+
+def test_backward_split_selection(fa_lib):
+    """Form 2 (two kernels) writes dQ directly and needs no workspace; form 1 needs
+    the fp32 dQ accumulator; d = 32 and 64 always use form 1."""
+    fa = fa_lib
+    try:
+        assert fa.fa_debug_set_bwd_split(3) == fa.FA_ERR_INVALID_ARG
+        assert fa.fa_debug_set_bwd_split(-1) == fa.FA_ERR_INVALID_ARG
+        assert fa.fa_debug_set_bwd_split(2) == fa.FA_OK
+        assert fa.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 0
+        assert fa.fa_bwd_workspace_size(2, 16, 4096, 64, 1) == 2 * 16 * 4096 * 64 * 4
+        assert fa.fa_debug_set_bwd_split(1) == fa.FA_OK
+        assert fa.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 2 * 16 * 4096 * 128 * 4
+    finally:
+        fa.fa_debug_set_bwd_split(0)
