@@ -14,4 +14,5 @@ from .attention import (  # noqa: F401
     rows_fwd_bwd,
     standard_attention_bwd,
     standard_attention_fwd,
+    visible_pairs,
 )

@@ -312,11 +312,11 @@ def _pins_hold():
 def test_pins_catch_a_flipped_mask(monkeypatch):
     orig = oa._scores
 
-    def flipped(q_rows, row_ids, K, causal, s):
+    def flipped(q_rows, row_ids, K, causal, s, off=0, window=0):
         S = (q_rows @ K.T) * s
         if causal:
             cols = np.arange(K.shape[0])[None, :]
-            S = np.where(cols < row_ids[:, None], -np.inf, S)  # wrong orientation
+            S = np.where(cols < row_ids[:, None] + off, -np.inf, S)  # wrong orientation
         return S
     assert _pins_hold()
     monkeypatch.setattr(oa, "_scores", flipped)
