@@ -18,6 +18,7 @@ import os
 __all__ = [
     "FA_OK", "FA_ERR_INVALID_ARG", "FA_ERR_UNSUPPORTED", "FA_ERR_CUDA", "FA_ERR_TIMEOUT", "FA_ERR_WORKSPACE",
     "FAError", "lib", "lib_path", "fa_fwd", "fa_bwd_preprocess", "fa_bwd_workspace_size", "fa_bwd",
+    "fa_fwd_ex", "fa_bwd_ex", "fa_bwd_workspace_size_ex", "fa_tile_pairs_ex",
     "fa_bwd_noalloc", "FA_NOALLOC_MAX_WORKSPACE_BYTES",
     "fa_status_string", "fa_get_tile_config", "fa_tile_pairs", "fa_debug_set_tile_counter", "fa_debug_set_bwd_split",
     "fa_poll_device_error", "fa_debug_timeout_probe", "fa_selftest_umma", "fa_version",
@@ -49,6 +50,10 @@ lib = _load()
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _sig = {
     "fa_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_bwd_workspace_size_ex": (_sz, [_i, _i, _i, _i, _i, _i, _i]),
+    "fa_bwd_ex": (_i, [_vp] * 10 + [_i] * 7 + [_f, _vp, _sz, _vp]),
+    "fa_tile_pairs_ex": (ctypes.c_longlong, [_i, _i, _i, _i, _i, _i]),
     "fa_bwd_preprocess": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
@@ -72,6 +77,24 @@ for _name, (_res, _args) in _sig.items():
 
 def fa_fwd(Q, K, V, O, L, B, H, N, d, causal, scale, stream):
     return lib.fa_fwd(Q, K, V, O, L, B, H, N, d, int(bool(causal)), scale, stream)
+
+
+def fa_fwd_ex(Q, K, V, O, L, B, H, Nq, Nk, d, causal, window, scale, stream):
+    return lib.fa_fwd_ex(Q, K, V, O, L, B, H, Nq, Nk, d, int(bool(causal)), window, scale, stream)
+
+
+def fa_bwd_workspace_size_ex(B, H, Nq, Nk, d, causal, window):
+    return lib.fa_bwd_workspace_size_ex(B, H, Nq, Nk, d, int(bool(causal)), window)
+
+
+def fa_bwd_ex(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, Nq, Nk, d, causal, window, scale, workspace, workspace_bytes,
+              stream):
+    return lib.fa_bwd_ex(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, Nq, Nk, d, int(bool(causal)), window, scale,
+                         workspace, workspace_bytes, stream)
+
+
+def fa_tile_pairs_ex(Nq, Nk, d, causal, window, pass_):
+    return lib.fa_tile_pairs_ex(Nq, Nk, d, int(bool(causal)), window, pass_)
 
 
 def fa_bwd_preprocess(O, dO, D, B, H, N, d, stream):
@@ -148,43 +171,52 @@ def _stream_handle(device):
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def _check_qkv(*ts):
+def _check_tensors(q, k, v, *rest):
+    """q [B,H,Nq,d], k and v [B,H,Nk,d], rest (o, do) like q: contiguous bf16 on one CUDA device."""
     import torch
-    t0 = ts[0]
-    for t in ts:
+    for t in (q, k, v) + rest:
         if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
             raise ValueError("expected contiguous bf16 CUDA tensors of shape [B, H, N, d]")
-        if t.shape != t0.shape or t.device != t0.device:
-            raise ValueError("Q, K, V (and O, dO) must share shape and device")
+        if t.device != q.device:
+            raise ValueError("all tensors must be on one device")
+    if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3]:
+        raise ValueError("K and V must be [B, H, Nk, d] with the B, H and d of Q")
+    for t in rest:
+        if t.shape != q.shape:
+            raise ValueError("O and dO must have the shape of Q")
 
 
-def attention_forward(q, k, v, causal=False, scale=None):
-    """O, L = exact attention of bf16 [B,H,N,d] CUDA tensors (L fp32 [B,H,N])."""
+def attention_forward(q, k, v, causal=False, scale=None, window=0):
+    """O, L = exact attention of bf16 CUDA tensors q [B,H,Nq,d], k, v [B,H,Nk,d]
+    (L fp32 [B,H,Nq]); the mask of fa_fwd_ex (queries at the last Nq positions,
+    optional sliding window)."""
     import torch
-    _check_qkv(q, k, v)
-    B, H, N, d = q.shape
+    _check_tensors(q, k, v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    check(fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, causal, scale,
-                 _stream_handle(q.device)), "fa_fwd")
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    check(fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d, causal,
+                    window, scale, _stream_handle(q.device)), "fa_fwd_ex")
     return o, lse
 
 
-def attention_backward(q, k, v, o, lse, do, causal=False, scale=None, workspace=None):
+def attention_backward(q, k, v, o, lse, do, causal=False, scale=None, window=0, workspace=None):
     """dQ, dK, dV (bf16) and D (fp32) of exact attention, from the forward's O and L."""
     import torch
-    _check_qkv(q, k, v, o, do)
-    B, H, N, d = q.shape
+    _check_tensors(q, k, v, o, do)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     stream = _stream_handle(q.device)
-    D = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    check(fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), D.data_ptr(), B, H, N, d, stream), "fa_bwd_preprocess")
-    ws_bytes = fa_bwd_workspace_size(B, H, N, d, causal)
+    D = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    check(fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), D.data_ptr(), B, H, Nq, d, stream), "fa_bwd_preprocess")
+    ws_bytes = fa_bwd_workspace_size_ex(B, H, Nq, Nk, d, causal, window)
     if workspace is None or workspace.numel() * workspace.element_size() < ws_bytes:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    check(fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                 D.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, causal, scale,
-                 workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream), "fa_bwd")
+    check(fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                    D.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, causal, window, scale,
+                    workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream), "fa_bwd_ex")
     return dq, dk, dv, D

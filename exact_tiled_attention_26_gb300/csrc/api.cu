@@ -64,6 +64,22 @@ fa_status check_shape(int B, int H, int N, int d, bool* empty) {
   return FA_OK;
 }
 
+// Shape and mask checks of the general-mask entry points.  *empty: no query rows
+// (or no heads), so no attention is computed.
+fa_status check_mask_shape(int B, int H, int Nq, int Nk, int d, int causal, int window, bool* empty) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || window < 0) return FA_ERR_INVALID_ARG;
+  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (window > 0 && !causal) return FA_ERR_INVALID_ARG;
+  const long long bh = static_cast<long long>(B) * H;
+  *empty = (bh == 0 || Nq == 0);
+  if (bh > 65535) return FA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(Nq) > (1LL << 30) || static_cast<long long>(Nk) > (1LL << 30)) return FA_ERR_UNSUPPORTED;
+  if (*empty) return FA_OK;
+  if (Nk == 0) return FA_ERR_INVALID_ARG;  // a softmax over no keys
+  if (causal && Nq > Nk) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
 bool check_scale(float scale) { return std::isfinite(scale) && scale > 0.f; }
 
 int current_device() {
@@ -148,30 +164,33 @@ fa_status fa_get_tile_config(int d, int pass, int* Br, int* Bc) {
   return FA_OK;
 }
 
-long long fa_tile_pairs(int N, int d, int causal, int pass) {
+long long fa_tile_pairs_ex(int Nq, int Nk, int d, int causal, int window, int pass) {
   int Br = 0, Bc = 0;
-  if (N < 0 || fa_get_tile_config(d, pass, &Br, &Bc) != FA_OK) return -1;
-  if (N == 0) return 0;
-  const long long Tq = (N + Br - 1) / Br, Tk = (N + Bc - 1) / Bc;
-  if (!causal) return Tq * Tk;
+  if (Nq < 0 || Nk < 0 || window < 0 || (window > 0 && !causal) || fa_get_tile_config(d, pass, &Br, &Bc) != FA_OK)
+    return -1;
+  if (Nq == 0 || Nk == 0) return 0;
+  if (causal && Nq > Nk) return -1;
+  const int Tq = (Nq + Br - 1) / Br;
   long long n = 0;
-  for (long long i = 0; i < Tq; ++i) {
-    const long long last = ((i + 1) * Br < N ? (i + 1) * Br : N) - 1;
-    const long long k = last / Bc + 1;
-    n += k < Tk ? k : Tk;
+  for (int i = 0; i < Tq; ++i) {
+    int lo = 0, hi = -1;
+    key_tile_range(i, Br, Bc, Nq, Nk, causal != 0, window, &lo, &hi);
+    if (hi >= lo) n += hi - lo + 1;
   }
   return n;
 }
+
+long long fa_tile_pairs(int N, int d, int causal, int pass) { return fa_tile_pairs_ex(N, N, d, causal, 0, pass); }
 
 fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter) {
   g_tile_counter = dev_counter;
   return FA_OK;
 }
 
-fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
-                 int causal, float scale, fa_stream_t stream) {
+fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Nq, int Nk,
+                    int d, int causal, int window, float scale, fa_stream_t stream) {
   bool empty = false;
-  fa_status st = check_shape(B, H, N, d, &empty);
+  fa_status st = check_mask_shape(B, H, Nq, Nk, d, causal, window, &empty);
   if (st != FA_OK) return st;
   if (!check_scale(scale)) return FA_ERR_INVALID_ARG;
   if (empty) return FA_OK;
@@ -180,8 +199,13 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
     return FA_ERR_INVALID_ARG;
   int* status = device_status_word();
   if (status == nullptr) return FA_ERR_CUDA;
-  FwdLaunch a{Q, K, V, O, L, B * H, N, d, causal ? 1 : 0, scale, stream, status, g_tile_counter};
+  FwdLaunch a{Q, K, V, O, L, B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
   return launch_fwd(a);
+}
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
+                 int causal, float scale, fa_stream_t stream) {
+  return fa_fwd_ex(Q, K, V, O, L, B, H, N, N, d, causal, 0, scale, stream);
 }
 
 fa_status fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int H, int N, int d,
@@ -202,12 +226,15 @@ static int bwd_split(int d) {
   return g_bwd_split != 0 ? g_bwd_split : kDefaultBwdSplitD128;
 }
 
-size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
-  (void)causal;
+size_t fa_bwd_workspace_size_ex(int B, int H, int Nq, int Nk, int d, int causal, int window) {
   bool empty = false;
-  if (check_shape(B, H, N, d, &empty) != FA_OK) return static_cast<size_t>(-1);
+  if (check_mask_shape(B, H, Nq, Nk, d, causal, window, &empty) != FA_OK) return static_cast<size_t>(-1);
   if (empty || bwd_split(d) == 2) return 0;
-  return static_cast<size_t>(B) * H * N * d * sizeof(float);
+  return static_cast<size_t>(B) * H * Nq * d * sizeof(float);
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
+  return fa_bwd_workspace_size_ex(B, H, N, N, d, causal, 0);
 }
 
 fa_status fa_debug_set_bwd_split(int split) {
@@ -216,32 +243,47 @@ fa_status fa_debug_set_bwd_split(int split) {
   return FA_OK;
 }
 
-fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
-                 const float* D, void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
-                 void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
+                    const float* D, void* dQ, void* dK, void* dV, int B, int H, int Nq, int Nk, int d, int causal,
+                    int window, float scale, void* workspace, size_t workspace_bytes, fa_stream_t stream) {
   bool empty = false;
-  fa_status st = check_shape(B, H, N, d, &empty);
+  fa_status st = check_mask_shape(B, H, Nq, Nk, d, causal, window, &empty);
   if (st != FA_OK) return st;
   if (!check_scale(scale)) return FA_ERR_INVALID_ARG;
-  if (empty) return FA_OK;
+  const size_t kv_bytes = static_cast<size_t>(B) * H * Nk * d * 2;
+  if (empty) {
+    // no query sees any key: the gradients of K and V are zero
+    if (kv_bytes == 0) return FA_OK;
+    if (!dK || !dV) return FA_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(dK, 0, kv_bytes, stream) != cudaSuccess || cudaMemsetAsync(dV, 0, kv_bytes, stream) != cudaSuccess)
+      return FA_ERR_CUDA;
+    return FA_OK;
+  }
   (void)O;  // O enters only through D = rowsum(dO * O), formed by fa_bwd_preprocess
   if (!Q || !K || !V || !dO || !L || !D || !dQ || !dK || !dV) return FA_ERR_INVALID_ARG;
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) || !aligned(dQ, 16) ||
       !aligned(dK, 16) || !aligned(dV, 16) || !aligned(L, 4) || !aligned(D, 4))
     return FA_ERR_INVALID_ARG;
-  const size_t need = fa_bwd_workspace_size(B, H, N, d, causal);
+  const size_t need = fa_bwd_workspace_size_ex(B, H, Nq, Nk, d, causal, window);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
     return FA_ERR_WORKSPACE;
   int* status = device_status_word();
   if (status == nullptr) return FA_ERR_CUDA;
-  BwdLaunch a{Q, K, V, dO, L, D, static_cast<float*>(workspace), dK, dV, B * H, N, d, causal ? 1 : 0, scale,
-              stream, status, g_tile_counter};
+  BwdLaunch a{Q,  K,  V,  dO, L,      D,     static_cast<float*>(workspace), dK,     dV,
+              B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
   if (bwd_split(d) == 2) return launch_bwd_two_kernel_d128(a, dQ);
   if (cudaMemsetAsync(workspace, 0, need, stream) != cudaSuccess) return FA_ERR_CUDA;
   st = launch_bwd(a);
   if (st != FA_OK) return st;
-  return launch_dq_convert(static_cast<const float*>(workspace), dQ, static_cast<long long>(B) * H * N * d, scale,
+  return launch_dq_convert(static_cast<const float*>(workspace), dQ, static_cast<long long>(B) * H * Nq * d, scale,
                            stream);
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* L,
+                 const float* D, void* dQ, void* dK, void* dV, int B, int H, int N, int d, int causal, float scale,
+                 void* workspace, size_t workspace_bytes, fa_stream_t stream) {
+  return fa_bwd_ex(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, N, N, d, causal, 0, scale, workspace, workspace_bytes,
+                   stream);
 }
 
 fa_status fa_poll_device_error(fa_stream_t stream, int* detail) {

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(256, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                const float* __restrict__ Lg, const float* __restrict__ Dg, float* __restrict__ dQacc,
-               __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int N, float c_log2, float scale,
+               __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int Nq, int Nk, int window, float c_log2, float scale,
                int* status, unsigned long long* tile_counter) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -88,9 +88,11 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kt = blockIdx.x;  // key tile; the longest causal loops come first
   const int bh = blockIdx.y;
-  const int Tq = (N + C::BM - 1) / C::BM;
-  const int i0 = CAUSAL ? (kt * C::BN) / C::BM : 0;  // first query tile with a visible entry
-  const int n_it = Tq - i0;
+  const int off = Nk - Nq;  // position of query row i is i + off
+  // visible query tiles i0 .. i0 + n_it - 1 (none: this CTA writes zero dK, dV)
+  int i0 = 0, ilast = 0;
+  query_tile_range(kt, C::BM, C::BN, Nq, Nk, CAUSAL, window, &i0, &ilast);
+  const int n_it = ilast >= i0 ? ilast - i0 + 1 : 0;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_KV), 1);
@@ -218,26 +220,30 @@ __global__ void __launch_bounds__(256, 1)
     float* Ds = Ls + C::BM;
     float* dQs = reinterpret_cast<float*>(smem + C::OFF_DQ);
     uint8_t* dSs = smem + C::OFF_DS;
-    const size_t row0 = static_cast<size_t>(bh) * N;
+    const size_t row0 = static_cast<size_t>(bh) * Nq, krow0 = static_cast<size_t>(bh) * Nk;
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
       const int q0 = (i0 + it) * C::BM;
-      // L (pre-multiplied by log2 e) and D of this query tile; rows past N get
+      // L (pre-multiplied by log2 e) and D of this query tile; rows past Nq get
       // L = +inf so that their P is exactly 0
       for (int t = ct; t < 2 * C::BM; t += 128) {
         const int r = t < C::BM ? t : t - C::BM;
         const int q = q0 + r;
         if (t < C::BM)
-          Ls[r] = q < N ? Lg[row0 + q] * kLog2e : INFINITY;
+          Ls[r] = q < Nq ? Lg[row0 + q] * kLog2e : INFINITY;
         else
-          Ds[r] = q < N ? Dg[row0 + q] : 0.f;
+          Ds[r] = q < Nq ? Dg[row0 + q] : 0.f;
       }
       named_bar_sync(1, 128);
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL), it & 1, guard, SITE_BWD_COMPUTE))) break;
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), it & 1, guard, SITE_BWD_COMPUTE))) break;
       tc_fence_after();
-      const bool masked = (CAUSAL && kt * C::BN + C::BN - 1 > q0) || (kt * C::BN + C::BN > N);
+      const bool masked = (CAUSAL && kt * C::BN + C::BN - 1 > q0 + off) ||
+                          (window > 0 && kt * C::BN <= q0 + C::BM - 1 + off - window) || (kt * C::BN + C::BN > Nk);
+      // queries of this tile (0 .. BM-1) that see this thread's key
+      const int qlo = CAUSAL ? key - off - q0 : 0;
+      const int qhi = key >= Nk ? -1 : (window > 0 ? key - off + window - 1 - q0 : C::BM - 1);
 #pragma unroll
       for (int c = 0; c < C::BM / 32; ++c) {
         uint32_t rs[32], rp[32];
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(256, 1)
           for (int y = 0; y < 2; ++y) {
             const int ql = 32 * c + x + y;  // query within the tile
             float p = ex2(fmaf(__uint_as_float(rs[x + y]), c_log2, -Ls[ql]));
-            if (masked && ((CAUSAL && key > q0 + ql) || key >= N)) p = 0.f;
+            if (masked && (ql < qlo || ql > qhi)) p = 0.f;
             const float ds = p * (__uint_as_float(rp[x + y]) - Ds[ql]);
             pv[y] = p;
             *reinterpret_cast<__nv_bfloat16*>(dSs + swz128_offset<C::BM>(ql, kr)) = __float2bfloat16_rn(ds);
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(256, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (ct == 0) {
-        const int rows = min(C::BM, N - q0);
+        const int rows = min(C::BM, Nq - q0);
         bulk_reduce_add_f32(dQacc + (row0 + q0) * D, smem_u32(dQs), static_cast<uint32_t>(rows * D * 4));
         bulk_commit();
       }
@@ -315,14 +321,18 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const uint32_t col = t == 0 ? C::TM_DK : C::TM_DV;
-        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (row0 + key) * D;
+        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (krow0 + key) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t r[32];
           tmem_ld32(tl + col + 32 * c, r);
           tmem_ld_wait<32>(r);
           const float f = t == 0 ? scale : 1.f;  // Eq 19's scale, applied once to dK
-          if (key < N) {
+          if (n_it == 0) {  // no query sees these keys: the accumulators were never written
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          if (key < Nk) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -352,16 +362,17 @@ template <int D, bool CAUSAL>
 fa_status launch_bwd_t(const BwdLaunch& a) {
   using C = BwdCfg<D>;
   CUtensorMap mQ, mK, mV, mdO;
-  if (!encode_bf16_3d(&mQ, a.Q, D, a.N, a.BH, C::CE, C::BM) || !encode_bf16_3d(&mdO, a.dO, D, a.N, a.BH, C::CE, C::BM) ||
-      !encode_bf16_3d(&mK, a.K, D, a.N, a.BH, C::CE, C::BN) || !encode_bf16_3d(&mV, a.V, D, a.N, a.BH, C::CE, C::BN))
+  if (!encode_bf16_3d(&mQ, a.Q, D, a.Nq, a.BH, C::CE, C::BM) ||
+      !encode_bf16_3d(&mdO, a.dO, D, a.Nq, a.BH, C::CE, C::BM) ||
+      !encode_bf16_3d(&mK, a.K, D, a.Nk, a.BH, C::CE, C::BN) || !encode_bf16_3d(&mV, a.V, D, a.Nk, a.BH, C::CE, C::BN))
     return FA_ERR_CUDA;
   auto kern = bwd_kernel<D, CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
-  const dim3 grid((a.N + C::BN - 1) / C::BN, a.BH);
+  const dim3 grid((a.Nk + C::BN - 1) / C::BN, a.BH);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   kern<<<grid, 256, C::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D, a.dQacc, static_cast<__nv_bfloat16*>(a.dK),
-                                         static_cast<__nv_bfloat16*>(a.dV), a.N, c_log2, a.scale, a.status,
+                                         static_cast<__nv_bfloat16*>(a.dV), a.Nq, a.Nk, a.window, c_log2, a.scale, a.status,
                                          a.counter);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

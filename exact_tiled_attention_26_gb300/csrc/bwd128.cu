@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     bwd_d128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const float* __restrict__ Lg, const float* __restrict__ Dg, float* __restrict__ dQacc,
-                    __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int N, float c_log2, float scale,
+                    __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int Nq, int Nk, int window, float c_log2, float scale,
                     int* status, unsigned long long* tile_counter) {
   using C = B128;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -99,10 +99,13 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kt = blockIdx.x;  // key tile: with the causal mask the longest loops come first
   const int bh = blockIdx.y;
-  const int Tq = (N + C::BM - 1) / C::BM;
-  const int i0 = CAUSAL ? kt : 0;  // first query tile with a visible entry (BM == BN)
-  const int n_it = Tq - i0;
-  const size_t row0 = static_cast<size_t>(bh) * N;
+  const int off = Nk - Nq;  // position of query row i is i + off
+  // visible query tiles i0 .. i0 + n_it - 1 (none: this CTA writes zero dK, dV)
+  int i0 = 0, ilast = 0;
+  query_tile_range(kt, C::BM, C::BN, Nq, Nk, CAUSAL, window, &i0, &ilast);
+  const int n_it = ilast >= i0 ? ilast - i0 + 1 : 0;
+  const size_t row0 = static_cast<size_t>(bh) * Nq;   // Q, dO, L, D, dQ rows
+  const size_t krow0 = static_cast<size_t>(bh) * Nk;  // K, V, dK, dV rows
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_KV), 1);
@@ -156,13 +159,13 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       const int s = it & 1;
       const int q0 = (i0 + it) * C::BM;
       // -L log2 e and D of this query tile, read before waiting for the stage; rows
-      // past N get -L log2 e = -inf so that their P is exactly 0
+      // past Nq get -L log2 e = -inf so that their P is exactly 0
       float lv[4], dv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int q = q0 + lane + 32 * u;
-        lv[u] = q < N ? -Lg[row0 + q] * kLog2e : -INFINITY;
-        dv[u] = q < N ? Dg[row0 + q] : 0.f;
+        lv[u] = q < Nq ? -Lg[row0 + q] * kLog2e : -INFINITY;
+        dv[u] = q < Nq ? Dg[row0 + q] : 0.f;
       }
       if (!mbar_wait_warp(bar(C::B_QEMPTY + s), ((it >> 1) & 1) ^ 1, guard, SITE_PRODUCER)) break;
       if (lane == 0) {
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       mbar_arrive(bar(C::B_DQCONS));
       const int q0 = (i0 + j) * C::BM;
       float* dst = dQacc + (row0 + q0) * C::D + dd;
-      const int nq = min(C::BM, N - q0);
+      const int nq = min(C::BM, Nq - q0);
       if (nq >= C::BM) {
 #pragma unroll
         for (int x = 0; x < C::BM; ++x) atomicAdd(dst + static_cast<size_t>(x) * C::D, __uint_as_float(r[x]));
@@ -311,7 +314,12 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       const int qh = (i0 + it) * C::BM + 64 * h;  // first query of this half
       const float4* L4 = reinterpret_cast<const float4*>(smem_raw + C::OFF_LD + s * C::LD_BYTES) + 16 * h;
       const float4* D4 = L4 + C::BM / 4;
-      const bool masked = (CAUSAL && kt * C::BN + C::BN - 1 > qh) || (kt * C::BN + C::BN > N);
+      const bool masked = (CAUSAL && kt * C::BN + C::BN - 1 > qh + off) ||
+                          (window > 0 && kt * C::BN <= qh + 63 + off - window) || (kt * C::BN + C::BN > Nk);
+      // queries of this half (0..63) that see this thread's key: key <= q + off (causal),
+      // key > q + off - window (window), and none at all past Nk
+      const int qlo = CAUSAL ? key - off - qh : 0;
+      const int qhi = key >= Nk ? -1 : (window > 0 ? key - off + window - 1 - qh : 63);
       const uint64_t cc = f2pack(c_log2, c_log2);
       // ---- P^T = 2^(S^T c - L log2 e), two sub-chunks of 32 queries, each released
       // to the dV product as soon as it is in tensor memory
@@ -337,9 +345,9 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
               p[y] = ex2(t0);
               p[y + 1] = ex2(t1);
               if (MASK) {
-                const int qx = qh + 32 * c + x;
-                if ((CAUSAL && key > qx) || key >= N) p[y] = 0.f;
-                if ((CAUSAL && key > qx + 1) || key >= N) p[y + 1] = 0.f;
+                const int xs = 32 * c + x;  // query of the half: visible iff qlo <= xs <= qhi
+                if (xs < qlo || xs > qhi) p[y] = 0.f;
+                if (xs + 1 < qlo || xs + 1 > qhi) p[y + 1] = 0.f;
               }
             }
             pk[16 * c + 2 * v] = pack_bf16x2(p[0], p[1]);
@@ -396,13 +404,17 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const float f = t == 0 ? scale : 1.f;
-        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (row0 + key) * C::D + 64 * h;
+        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (krow0 + key) * C::D + 64 * h;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
           tmem_ld32(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 64 * h + 32 * c, r);
           tmem_ld_wait<32>(r);
-          if (key < N) {
+          if (n_it == 0) {  // no query sees these keys: the accumulators were never written
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          if (key < Nk) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -436,17 +448,18 @@ template <bool CAUSAL>
 fa_status launch_t(const BwdLaunch& a) {
   using C = B128;
   CUtensorMap mQ, mK, mV, mdO;
-  if (!encode_bf16_3d(&mQ, a.Q, C::D, a.N, a.BH, 64, C::BM) || !encode_bf16_3d(&mdO, a.dO, C::D, a.N, a.BH, 64, C::BM) ||
-      !encode_bf16_3d(&mK, a.K, C::D, a.N, a.BH, 64, C::BN) || !encode_bf16_3d(&mV, a.V, C::D, a.N, a.BH, 64, C::BN))
+  if (!encode_bf16_3d(&mQ, a.Q, C::D, a.Nq, a.BH, 64, C::BM) ||
+      !encode_bf16_3d(&mdO, a.dO, C::D, a.Nq, a.BH, 64, C::BM) ||
+      !encode_bf16_3d(&mK, a.K, C::D, a.Nk, a.BH, 64, C::BN) || !encode_bf16_3d(&mV, a.V, C::D, a.Nk, a.BH, 64, C::BN))
     return FA_ERR_CUDA;
   auto kern = bwd_d128_kernel<CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
-  const dim3 grid((a.N + C::BN - 1) / C::BN, a.BH);
+  const dim3 grid((a.Nk + C::BN - 1) / C::BN, a.BH);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   kern<<<grid, C::NTHREADS, C::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D, a.dQacc,
                                                  static_cast<__nv_bfloat16*>(a.dK), static_cast<__nv_bfloat16*>(a.dV),
-                                                 a.N, c_log2, a.scale, a.status, a.counter);
+                                                 a.Nq, a.Nk, a.window, c_log2, a.scale, a.status, a.counter);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

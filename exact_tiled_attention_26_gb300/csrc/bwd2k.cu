@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const float* __restrict__ Lg, const float* __restrict__ Dg, __nv_bfloat16* __restrict__ dK,
-                  __nv_bfloat16* __restrict__ dV, int N, float c_log2, float scale, int* status,
+                  __nv_bfloat16* __restrict__ dV, int Nq, int Nk, int window, float c_log2, float scale, int* status,
                   unsigned long long* tile_counter) {
   using C = KVC;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -64,10 +64,11 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
   const Guard guard{status, abort_flag};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kt = blockIdx.x, bh = blockIdx.y;
-  const int Tq = (N + 127) / 128;
-  const int i0 = CAUSAL ? kt : 0;
-  const int n_it = Tq - i0;
-  const size_t row0 = static_cast<size_t>(bh) * N;
+  const int off = Nk - Nq;  // position of query row i is i + off
+  int i0 = 0, ilast = 0;
+  query_tile_range(kt, 128, 128, Nq, Nk, CAUSAL, window, &i0, &ilast);
+  const int n_it = ilast >= i0 ? ilast - i0 + 1 : 0;  // none: this CTA writes zero dK, dV
+  const size_t row0 = static_cast<size_t>(bh) * Nq, krow0 = static_cast<size_t>(bh) * Nk;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_KV), 1);
@@ -112,8 +113,8 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int q = q0 + lane + 32 * u;
-        lv[u] = q < N ? -Lg[row0 + q] * kLog2e : -INFINITY;
-        dv[u] = q < N ? Dg[row0 + q] : 0.f;
+        lv[u] = q < Nq ? -Lg[row0 + q] * kLog2e : -INFINITY;
+        dv[u] = q < Nq ? Dg[row0 + q] : 0.f;
       }
       if (!mbar_wait_warp(bar(C::B_QEMPTY + s), ((it >> 1) & 1) ^ 1, guard, SITE_KV)) break;
       if (lane == 0) {
@@ -214,7 +215,11 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
       const int qh = (i0 + it) * 128 + 64 * h;
       const float4* L4 = reinterpret_cast<const float4*>(smem_raw + C::OFF_LD + s * C::LD_BYTES) + 16 * h;
       const float4* D4 = L4 + 32;
-      const bool masked = (CAUSAL && kt * 128 + 127 > qh) || (kt * 128 + 128 > N);
+      const bool masked = (CAUSAL && kt * 128 + 127 > qh + off) || (window > 0 && kt * 128 <= qh + 63 + off - window) ||
+                          (kt * 128 + 128 > Nk);
+      // queries of this half (0..63) that see this thread's key
+      const int qlo = CAUSAL ? key - off - qh : 0;
+      const int qhi = key >= Nk ? -1 : (window > 0 ? key - off + window - 1 - qh : 63);
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -237,9 +242,9 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
               p[y] = ex2(t0);
               p[y + 1] = ex2(t1);
               if (MASK) {
-                const int qx = qh + 32 * c + x;
-                if ((CAUSAL && key > qx) || key >= N) p[y] = 0.f;
-                if ((CAUSAL && key > qx + 1) || key >= N) p[y + 1] = 0.f;
+                const int xs = 32 * c + x;  // query of the half: visible iff qlo <= xs <= qhi
+                if (xs < qlo || xs > qhi) p[y] = 0.f;
+                if (xs + 1 < qlo || xs + 1 > qhi) p[y + 1] = 0.f;
               }
             }
             pk[16 * c + 2 * v] = pack_bf16x2(p[0], p[1]);
@@ -293,13 +298,17 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const float f = t == 0 ? scale : 1.f;
-        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (row0 + key) * 128 + 64 * h;
+        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (krow0 + key) * 128 + 64 * h;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
           tmem_ld32(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 64 * h + 32 * c, r);
           tmem_ld_wait<32>(r);
-          if (key < N) {
+          if (n_it == 0) {  // no query sees these keys: the accumulators were never written
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          }
+          if (key < Nk) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -350,7 +359,7 @@ template <bool CAUSAL>
 __global__ void __launch_bounds__(QC::NTHREADS, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                 const float* __restrict__ Lg, const float* __restrict__ Dg, __nv_bfloat16* __restrict__ dQ, int N,
+                 const float* __restrict__ Lg, const float* __restrict__ Dg, __nv_bfloat16* __restrict__ dQ, int Nq, int Nk, int window,
                  float c_log2, float scale, int* status) {
   using C = QC;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -361,11 +370,14 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + C::OFF_MISC + 4);
   const Guard guard{status, abort_flag};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = (N + 127) / 128;
+  const int T = (Nq + 127) / 128;
   const int qt = T - 1 - static_cast<int>(blockIdx.x);  // longest causal rows first
   const int bh = blockIdx.y;
-  const int n_kv = CAUSAL ? min(T, (min((qt + 1) * 128, N) - 1) / 128 + 1) : T;
-  const size_t row0 = static_cast<size_t>(bh) * N;
+  const int off = Nk - Nq;
+  int jlo = 0, jhi = 0;  // visible key tiles (every query row sees at least one key)
+  key_tile_range(qt, 128, 128, Nq, Nk, CAUSAL, window, &jlo, &jhi);
+  const int n_kv = jhi - jlo + 1;
+  const size_t row0 = static_cast<size_t>(bh) * Nq;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QDO), 1);
@@ -409,12 +421,12 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
       if (!mbar_wait(bar(C::B_KEMPTY + k), ((j / C::KST) & 1) ^ 1, guard, SITE_Q)) break;
       mbar_expect_tx(bar(C::B_KFULL + k), TILE);
       for (int c = 0; c < 2; ++c)
-        tma_load_3d(tb + C::T_K + k * TILE + c * 128 * 128, &tmK, bar(C::B_KFULL + k), c * 64, j * 128, bh);
+        tma_load_3d(tb + C::T_K + k * TILE + c * 128 * 128, &tmK, bar(C::B_KFULL + k), c * 64, (jlo + j) * 128, bh);
       lastk = j;
       if (!mbar_wait(bar(C::B_VEMPTY + v), ((j >> 1) & 1) ^ 1, guard, SITE_Q)) break;
       mbar_expect_tx(bar(C::B_VFULL + v), TILE);
       for (int c = 0; c < 2; ++c)
-        tma_load_3d(tb + C::T_V + v * TILE + c * 128 * 128, &tmV, bar(C::B_VFULL + v), c * 64, j * 128, bh);
+        tma_load_3d(tb + C::T_V + v * TILE + c * 128 * 128, &tmV, bar(C::B_VFULL + v), c * 64, (jlo + j) * 128, bh);
       lastv = j;
     }
     if (*abort_flag) {
@@ -477,16 +489,21 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
     // ---------------------------------------------------------------- element-wise warps
     const int qw = warp & 3, h = (warp - 4) >> 2, row = qw * 32 + lane, q = qt * 128 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
-    const float nl = q < N ? -Lg[row0 + q] * kLog2e : -INFINITY;  // rows past N: P = 0
-    const float dq = q < N ? Dg[row0 + q] : 0.f;
+    const float nl = q < Nq ? -Lg[row0 + q] * kLog2e : -INFINITY;  // rows past Nq: P = 0
+    const float dq = q < Nq ? Dg[row0 + q] : 0.f;
+    const int p = q + off;  // this row's position
     const uint64_t cc = f2pack(c_log2, c_log2), nl2 = f2pack(nl, nl), nd2 = f2pack(-dq, -dq);
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int s = j & 1;
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL + s), (j >> 1) & 1, guard, SITE_Q))) break;
       tc_fence_after();
-      const int kh = j * 128 + 64 * h;  // first key of this half
-      const bool masked = (CAUSAL && kh + 63 > qt * 128) || (kh + 64 > N);
+      const int kh = (jlo + j) * 128 + 64 * h;  // first key of this half
+      const bool masked = (CAUSAL && kh + 63 > qt * 128 + off) || (window > 0 && kh <= qt * 128 + 127 + off - window) ||
+                          (kh + 64 > Nk);
+      // keys of this half (0..63) this row sees: position p, keys below Nk
+      const int khi = min(CAUSAL ? p - kh : 63, Nk - 1 - kh);
+      const int klo = window > 0 ? p - window + 1 - kh : 0;
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -501,9 +518,9 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
             f2unpack(ffma2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), cc, nl2), t0, t1);
             float p0 = ex2(t0), p1 = ex2(t1);
             if (MASK) {
-              const int k = kh + 32 * c + x;
-              if ((CAUSAL && k > q) || k >= N) p0 = 0.f;
-              if ((CAUSAL && k + 1 > q) || k + 1 >= N) p1 = 0.f;
+              const int xs = 32 * c + x;  // key of the half: visible iff klo <= xs <= khi
+              if (xs < klo || xs > khi) p0 = 0.f;
+              if (xs + 1 < klo || xs + 1 > khi) p1 = 0.f;
             }
             pk[16 * c + (x >> 1)] = pack_bf16x2(p0, p1);
           }
@@ -547,7 +564,7 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
         uint32_t r[32];
         tmem_ld32(tl + C::TM_DQ + 64 * h + 32 * c, r);
         tmem_ld_wait<32>(r);
-        if (q < N) {
+        if (q < Nq) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
@@ -577,8 +594,8 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
 template <bool CAUSAL>
 fa_status launch_t(const BwdLaunch& a, void* dQ) {
   CUtensorMap mQ, mK, mV, mdO;
-  if (!encode_bf16_3d(&mQ, a.Q, 128, a.N, a.BH, 64, 128) || !encode_bf16_3d(&mdO, a.dO, 128, a.N, a.BH, 64, 128) ||
-      !encode_bf16_3d(&mK, a.K, 128, a.N, a.BH, 64, 128) || !encode_bf16_3d(&mV, a.V, 128, a.N, a.BH, 64, 128))
+  if (!encode_bf16_3d(&mQ, a.Q, 128, a.Nq, a.BH, 64, 128) || !encode_bf16_3d(&mdO, a.dO, 128, a.Nq, a.BH, 64, 128) ||
+      !encode_bf16_3d(&mK, a.K, 128, a.Nk, a.BH, 64, 128) || !encode_bf16_3d(&mV, a.V, 128, a.Nk, a.BH, 64, 128))
     return FA_ERR_CUDA;
   static_assert(KVC::SMEM <= SMEM_MAX && QC::SMEM <= SMEM_MAX, "shared memory budget");
   auto kkv = bwd_kv_kernel<CAUSAL>;
@@ -586,15 +603,15 @@ fa_status launch_t(const BwdLaunch& a, void* dQ) {
   if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, KVC::SMEM) != cudaSuccess ||
       cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, QC::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
-  const int T = (a.N + 127) / 128;
+  const int Tq = (a.Nq + 127) / 128, Tk = (a.Nk + 127) / 128;
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  kkv<<<dim3(T, a.BH), KVC::NTHREADS, KVC::SMEM, a.stream>>>(
-      mQ, mK, mV, mdO, a.L, a.D, static_cast<__nv_bfloat16*>(a.dK), static_cast<__nv_bfloat16*>(a.dV), a.N, c_log2,
-      a.scale, a.status, a.counter);
+  kkv<<<dim3(Tk, a.BH), KVC::NTHREADS, KVC::SMEM, a.stream>>>(
+      mQ, mK, mV, mdO, a.L, a.D, static_cast<__nv_bfloat16*>(a.dK), static_cast<__nv_bfloat16*>(a.dV), a.Nq, a.Nk,
+      a.window, c_log2, a.scale, a.status, a.counter);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  kq<<<dim3(T, a.BH), QC::NTHREADS, QC::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D,
-                                                          static_cast<__nv_bfloat16*>(dQ), a.N, c_log2, a.scale,
-                                                          a.status);
+  kq<<<dim3(Tq, a.BH), QC::NTHREADS, QC::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D,
+                                                           static_cast<__nv_bfloat16*>(dQ), a.Nq, a.Nk, a.window,
+                                                           c_log2, a.scale, a.status);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

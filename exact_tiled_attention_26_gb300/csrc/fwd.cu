@@ -65,7 +65,7 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ Lout,
-               int N, float c_log2, int* status, unsigned long long* tile_counter) {
+               int Nq, int Nk, int window, float c_log2, int* status, unsigned long long* tile_counter) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -76,11 +76,14 @@ __global__ void __launch_bounds__(256, 1)
   const Guard guard{status, abort_flag};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int T = (N + C::BM - 1) / C::BM;
+  const int T = (Nq + C::BM - 1) / C::BM;
   const int qt = T - 1 - static_cast<int>(blockIdx.x);  // longest causal rows first
   const int bh = blockIdx.y;
-  int n_kv = T;
-  if (CAUSAL) n_kv = min(T, (min((qt + 1) * C::BM, N) - 1) / C::BN + 1);
+  const int off = Nk - Nq;  // position of query row i is i + off
+  // visible key tiles jlo .. jlo + n_kv - 1 (whole-tile skip on both sides of the band)
+  int jlo = 0, jhi = 0;
+  key_tile_range(qt, C::BM, C::BN, Nq, Nk, CAUSAL, window, &jlo, &jhi);
+  const int n_kv = jhi - jlo + 1;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_Q), 1);
@@ -128,13 +131,13 @@ __global__ void __launch_bounds__(256, 1)
       mbar_expect_tx(bar(C::B_KFULL + s), C::TILE);
       for (int c = 0; c < C::NCH; ++c)
         tma_load_3d(sb + C::OFF_K + s * C::TILE + c * C::BN * C::SWB, &tmK, bar(C::B_KFULL + s), c * C::CE,
-                    j * C::BN, bh);
+                    (jlo + j) * C::BN, bh);
       jk = j;
       if (!mbar_wait(bar(C::B_VEMPTY + s), par, guard, SITE_FWD_PRODUCER)) break;
       mbar_expect_tx(bar(C::B_VFULL + s), C::TILE);
       for (int c = 0; c < C::NCH; ++c)
         tma_load_3d(sb + C::OFF_V + s * C::TILE + c * C::BN * C::SWB, &tmV, bar(C::B_VFULL + s), c * C::CE,
-                    j * C::BN, bh);
+                    (jlo + j) * C::BN, bh);
       jv = j;
     }
     if (*abort_flag) {
@@ -204,13 +207,15 @@ __global__ void __launch_bounds__(256, 1)
       float s[128];
 #pragma unroll
       for (int k = 0; k < 128; ++k) s[k] = __uint_as_float(r[k]);
-      const int k0 = j * C::BN;
-      if ((CAUSAL && k0 + C::BN - 1 > qt * C::BM) || k0 + C::BN > N) {
+      const int k0 = (jlo + j) * C::BN;
+      if ((CAUSAL && k0 + C::BN - 1 > qt * C::BM + off) || (window > 0 && k0 <= qt * C::BM + C::BM - 1 + off - window) ||
+          k0 + C::BN > Nk) {
+        // this row sees tile columns lo .. hi (position q + off; keys below Nk)
+        const int hi = min(CAUSAL ? q + off - k0 : C::BN - 1, Nk - 1 - k0);
+        const int lo = window > 0 ? q + off - window + 1 - k0 : 0;
 #pragma unroll
-        for (int k = 0; k < 128; ++k) {
-          const int key = k0 + k;
-          if ((CAUSAL && key > q) || key >= N) s[k] = -INFINITY;
-        }
+        for (int k = 0; k < 128; ++k)
+          if (k > hi || k < lo) s[k] = -INFINITY;
       }
       float mx = s[0];
 #pragma unroll
@@ -245,7 +250,9 @@ __global__ void __launch_bounds__(256, 1)
           tmem_st_wait();
         }
       }
-      const float neg_m = -m_run;
+      // a row whose keys so far were all masked (a window's first tile) keeps
+      // m = -inf; its P is 0 and the first visible tile rescales by 0
+      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
       float lsum0 = 0.f, lsum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
       uint32_t p[64];
 #pragma unroll
@@ -273,7 +280,7 @@ __global__ void __launch_bounds__(256, 1)
       // O is normalised by the sum of the very bf16 weights that entered P V, so
       // that the weights applied to V sum to one; L uses the unrounded sum.
       const float inv_l = 1.f / lr_run;
-      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + q) * D;
+      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * Nq + q) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -283,13 +290,13 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (q < N) {
+        if (q < Nq) {
           uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
-      if (q < N) Lout[static_cast<size_t>(bh) * N + q] = (m_run + lg2(l_run)) * kLn2;
+      if (q < Nq) Lout[static_cast<size_t>(bh) * Nq + q] = (m_run + lg2(l_run)) * kLn2;
     }
   }
 
@@ -313,16 +320,16 @@ template <int D, bool CAUSAL>
 fa_status launch_fwd_t(const FwdLaunch& a) {
   using C = FwdCfg<D>;
   CUtensorMap mQ, mK, mV;
-  if (!encode_bf16_3d(&mQ, a.Q, D, a.N, a.BH, C::CE, C::BM) || !encode_bf16_3d(&mK, a.K, D, a.N, a.BH, C::CE, C::BN) ||
-      !encode_bf16_3d(&mV, a.V, D, a.N, a.BH, C::CE, C::BN))
+  if (!encode_bf16_3d(&mQ, a.Q, D, a.Nq, a.BH, C::CE, C::BM) ||
+      !encode_bf16_3d(&mK, a.K, D, a.Nk, a.BH, C::CE, C::BN) || !encode_bf16_3d(&mV, a.V, D, a.Nk, a.BH, C::CE, C::BN))
     return FA_ERR_CUDA;
   auto kern = fwd_kernel<D, CAUSAL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
-  const dim3 grid((a.N + C::BM - 1) / C::BM, a.BH);
+  const dim3 grid((a.Nq + C::BM - 1) / C::BM, a.BH);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  kern<<<grid, 256, C::SMEM, a.stream>>>(mQ, mK, mV, static_cast<__nv_bfloat16*>(a.O), a.L, a.N, c_log2, a.status,
-                                         a.counter);
+  kern<<<grid, 256, C::SMEM, a.stream>>>(mQ, mK, mV, static_cast<__nv_bfloat16*>(a.O), a.L, a.Nq, a.Nk, a.window,
+                                         c_log2, a.status, a.counter);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -15,6 +15,45 @@ constexpr int kFwdBr = 128, kFwdBc = 128;
 constexpr int kBwdBc = 128;
 constexpr int bwd_br(int) { return 128; }
 
+// Visible tile ranges of the mask (FwdLaunch), shared by host counts and kernels.
+// Key tiles [*lo, *hi] seen by query tile qt (Br rows), and query tiles seen by key
+// tile kt (Bc keys); an empty range has *hi < *lo.
+__host__ __device__ inline void key_tile_range(int qt, int Br, int Bc, int Nq, int Nk, bool causal, int window,
+                                               int* lo, int* hi) {
+  const int off = Nk - Nq;
+  const int Tk = (Nk + Bc - 1) / Bc;
+  const int p_first = qt * Br + off;
+  const int p_last = (qt * Br + Br < Nq ? qt * Br + Br : Nq) - 1 + off;
+  int h = Tk - 1;
+  if (causal && p_last / Bc < h) h = p_last / Bc;
+  int l = 0;
+  if (window > 0) {
+    const int first_key = p_first - window + 1;
+    l = first_key > 0 ? first_key / Bc : 0;
+  }
+  *lo = l;
+  *hi = h;
+}
+__host__ __device__ inline void query_tile_range(int kt, int Br, int Bc, int Nq, int Nk, bool causal, int window,
+                                                 int* lo, int* hi) {
+  const int off = Nk - Nq;
+  const int Tq = (Nq + Br - 1) / Br;
+  const int k_first = kt * Bc;
+  const int k_last = (kt * Bc + Bc < Nk ? kt * Bc + Bc : Nk) - 1;
+  int l = 0;
+  if (causal) {
+    const int first_row = k_first - off;  // first query whose position reaches this tile
+    l = first_row > 0 ? first_row / Br : 0;
+  }
+  int h = Tq - 1;
+  if (window > 0) {
+    const int last_row = k_last - off + window - 1;  // last query whose window still reaches it
+    h = last_row < 0 ? -1 : (last_row / Br < h ? last_row / Br : h);
+  }
+  *lo = l;
+  *hi = h;
+}
+
 // Device status word of the current device (see fa_poll_device_error).
 int* device_status_word();
 
@@ -25,11 +64,14 @@ bool encode_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int BH, in
 bool encode_bf16_2d(CUtensorMap* map, const void* base, int inner_total, int rows_total, int box_inner,
                     int box_rows);
 
+// Mask of every pass: Q (and O, L, dO, D, dQ) have Nq rows per head, K and V
+// (and dK, dV) Nk rows; query row i sits at position i + Nk - Nq.  causal: keys
+// j <= position; window > 0 (only with causal): also j > position - window.
 struct FwdLaunch {
   const void *Q, *K, *V;
   void* O;
   float* L;
-  int BH, N, d, causal;
+  int BH, Nq, Nk, d, causal, window;
   float scale;
   cudaStream_t stream;
   int* status;
@@ -42,7 +84,7 @@ struct BwdLaunch {
   const float *L, *D;
   float* dQacc;
   void *dK, *dV;
-  int BH, N, d, causal;
+  int BH, Nq, Nk, d, causal, window;
   float scale;
   cudaStream_t stream;
   int* status;

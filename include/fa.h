@@ -67,6 +67,29 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L,
                  int B, int H, int N, int d, int causal, float scale, fa_stream_t stream);
 
 /*
+ * Forward pass with a general mask ("_ex" forms take Nq and Nk separately and a
+ * sliding window; fa_fwd is fa_fwd_ex with Nq = Nk = N and window = 0).
+ *   Q       : in,  bf16 [B,H,Nq,d]      K, V : in, bf16 [B,H,Nk,d]
+ *   O       : out, bf16 [B,H,Nq,d]      L    : out, fp32 [B,H,Nq]
+ * Query row i sits at sequence position i + Nk - Nq: the queries are the last
+ * Nq positions of the key sequence, so a decoded token (Nq = 1) sees every key
+ * ("CS349E lecture 11: 03_flash_backward.py" demo4_causal, observation 3);
+ * with Nq = Nk this is the top-left alignment of fa_fwd.
+ *   causal : query i sees keys j <= i + Nk - Nq; needs Nq <= Nk
+ *            (FA_ERR_UNSUPPORTED otherwise).
+ *   window : 0 for none; w > 0 (only with causal, else FA_ERR_INVALID_ARG):
+ *            query i also sees only keys j > i + Nk - Nq - w, i.e. itself and
+ *            the w - 1 positions before it ("CS324 lecture 8:
+ *            03_online_softmax_and_flash.py" window_attention_torch).  Key
+ *            tiles wholly outside the band are skipped on both sides.
+ * Nq = 0 is a no-op; Nk = 0 with Nq > 0 is FA_ERR_INVALID_ARG (a softmax over
+ * no keys).  Every other argument as in fa_fwd.
+ */
+fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L,
+                    int B, int H, int Nq, int Nk, int d, int causal, int window, float scale,
+                    fa_stream_t stream);
+
+/*
  * Backward preprocessing: D_i = sum_k dO_ik * O_ik (fp32 accumulation).
  * "CS336 Assignment 2 notes" §1.4 Eq 17 (D = rowsum(O * dO)); the identity
  * D_i = sum_j dP_ij P_ij that lets D be formed once before the backward is
@@ -103,6 +126,19 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
                  const float* L, const float* D, void* dQ, void* dK, void* dV,
                  int B, int H, int N, int d, int causal, float scale,
                  void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
+/*
+ * Backward pass with the general mask of fa_fwd_ex (same Nq, Nk, causal,
+ * window; L, D, dQ are [B,H,Nq], [B,H,Nq], [B,H,Nq,d]; dK, dV [B,H,Nk,d]).
+ * Keys that no query sees get dK = dV = 0; Nq = 0 writes zeros to dK and dV.
+ * The workspace is fa_bwd_workspace_size_ex() bytes.  fa_bwd is fa_bwd_ex with
+ * Nq = Nk = N and window = 0.
+ */
+size_t fa_bwd_workspace_size_ex(int B, int H, int Nq, int Nk, int d, int causal, int window);
+fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                    const float* L, const float* D, void* dQ, void* dK, void* dV,
+                    int B, int H, int Nq, int Nk, int d, int causal, int window, float scale,
+                    void* workspace, size_t workspace_bytes, fa_stream_t stream);
 
 /*
  * Largest workspace fa_bwd_noalloc can provide: B*H*N*d*4 bytes must not exceed
@@ -151,6 +187,14 @@ fa_status fa_get_tile_config(int d, int pass, int* Br, int* Bc);
  * "CS349E lecture 11" demo4_causal).  Host only; -1 on bad arguments.
  */
 long long fa_tile_pairs(int N, int d, int causal, int pass);
+
+/*
+ * The same count for the mask of fa_fwd_ex: query tile i (positions p_first ..
+ * p_last) sees key tiles max(0, floor((p_first - w + 1) / Bc)) .. floor(p_last /
+ * Bc) (the first bound only with a window w, the second only when causal).
+ * Host only; -1 on bad arguments.
+ */
+long long fa_tile_pairs_ex(int Nq, int Nk, int d, int causal, int window, int pass);
 
 /*
  * Debug: when `dev_counter` is non-NULL, every later fa_fwd / fa_bwd launch

@@ -51,36 +51,37 @@ def lib():
     return fa
 
 
-def run_gpu(Q, K, V, dO, causal, scale=None, counter=False, split=0):
-    """Forward + preprocess + backward through the C ABI.  Inputs: bf16 CPU tensors
-    [B,H,N,d].  `split` selects the backward form (fa_debug_set_bwd_split; 0 =
-    the library's default).  Returns CPU tensors and (if asked) the tile-pair
-    counts."""
+def run_gpu(Q, K, V, dO, causal, scale=None, counter=False, split=0, window=0):
+    """Forward + preprocess + backward through the C ABI (the general-mask entry
+    points).  Inputs: bf16 CPU tensors Q, dO [B,H,Nq,d], K, V [B,H,Nk,d].  `split`
+    selects the backward form (fa_debug_set_bwd_split; 0 = the library's default).
+    Returns CPU tensors and (if asked) the tile-pair counts."""
     fa = lib()
     fa.check(fa.fa_debug_set_bwd_split(split))
-    B, H, N, d = Q.shape
+    B, H, Nq, d = Q.shape
+    Nk = K.shape[2]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     dev = torch.device("cuda")
     q, k, v, do = (t.to(dev) for t in (Q, K, V, dO))
     o = torch.empty_like(q)
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-    D = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+    D = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d, causal)
+    ws_bytes = fa.fa_bwd_workspace_size_ex(B, H, Nq, Nk, d, causal, window)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     cnt = torch.zeros(2, dtype=torch.int64, device=dev)
     s = stream()
     if counter:
         fa.check(fa.fa_debug_set_tile_counter(cnt.data_ptr()))
     try:
-        fa.check(fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
-                           causal, scale, s), "fa_fwd")
+        fa.check(fa.fa_fwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d,
+                              causal, window, scale, s), "fa_fwd_ex")
         if counter:
             fa.check(fa.fa_debug_set_tile_counter(cnt.data_ptr() + 8))
-        fa.check(fa.fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), D.data_ptr(), B, H, N, d, s), "preprocess")
-        fa.check(fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                           D.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, causal, scale,
-                           ws.data_ptr(), ws.numel(), s), "fa_bwd")
+        fa.check(fa.fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), D.data_ptr(), B, H, Nq, d, s), "preprocess")
+        fa.check(fa.fa_bwd_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                              D.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, causal, window,
+                              scale, ws.data_ptr(), ws.numel(), s), "fa_bwd_ex")
     finally:
         fa.fa_debug_set_bwd_split(0)
         if counter:

@@ -127,3 +127,36 @@ def test_backward_split_selection(fa_lib):
         assert fa.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 2 * 16 * 4096 * 128 * 4
     finally:
         fa.fa_debug_set_bwd_split(0)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 1), (1, 1000), (7, 300), (128, 1000), (300, 1000), (1000, 1000), (129, 257),
+                                   (8192, 8192), (32768, 32768), (4096, 8192)])
+@pytest.mark.parametrize("window", [0, 1, 64, 127, 128, 129, 500, 1024])
+@pytest.mark.parametrize("d", [64, 128])
+def test_masked_tile_pairs_match_oracle(fa_lib, Nq, Nk, window, d):
+    """The library's two-sided tile ranges give the oracle's count for every pass
+    (query tiles outer and key tiles outer visit the same set of pairs)."""
+    for pass_ in (0, 1):
+        _, br, bc = fa_lib.fa_get_tile_config(d, pass_)
+        assert fa_lib.fa_tile_pairs_ex(Nq, Nk, d, True, window, pass_) == \
+            oracle.causal_tile_pairs(Nq, br, bc, True, Nk=Nk, window=window)
+        if window == 0:
+            assert fa_lib.fa_tile_pairs_ex(Nq, Nk, d, False, 0, pass_) == \
+                oracle.causal_tile_pairs(Nq, br, bc, False, Nk=Nk)
+
+
+def test_masked_argument_errors(fa_lib):
+    fa = fa_lib
+    p = 4096
+    assert fa.fa_fwd_ex(p, p, p, p, p, 1, 1, 64, 64, 64, 0, 16, 0.1, None) == fa.FA_ERR_INVALID_ARG  # window w/o causal
+    assert fa.fa_fwd_ex(p, p, p, p, p, 1, 1, 64, 64, 64, 1, -1, 0.1, None) == fa.FA_ERR_INVALID_ARG  # negative window
+    assert fa.fa_fwd_ex(p, p, p, p, p, 1, 1, 65, 64, 64, 1, 0, 0.1, None) == fa.FA_ERR_UNSUPPORTED  # causal Nq > Nk
+    assert fa.fa_fwd_ex(p, p, p, p, p, 1, 1, 64, 0, 64, 0, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG  # no keys
+    assert fa.fa_fwd_ex(None, None, None, None, None, 1, 1, 0, 64, 64, 1, 8, 0.1, None) == fa.FA_OK  # no queries
+    assert fa.fa_tile_pairs_ex(65, 64, 128, 1, 0, 0) == -1
+    assert fa.fa_tile_pairs_ex(64, 64, 128, 0, 8, 0) == -1
+    assert fa.fa_bwd_workspace_size_ex(2, 3, 100, 700, 64, 1, 50) == 2 * 3 * 100 * 64 * 4
+    assert fa.fa_bwd_workspace_size_ex(2, 3, 100, 700, 64, 0, 50) == ctypes.c_size_t(-1).value
+    for N, c in ((1000, 0), (1000, 1), (129, 1)):
+        for pass_ in (0, 1):
+            assert fa.fa_tile_pairs_ex(N, N, 128, c, 0, pass_) == fa.fa_tile_pairs(N, 128, c, pass_)
