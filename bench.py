@@ -41,7 +41,7 @@ UNIT = "TFLOP/s"
 # backward main kernel, from the ncu capture summarised in
 # profiles/launches_vlong_1x32x32768x128_causal.md; valid for the kernel as captured
 # there (set to None whenever the kernel changes).
-_TRAFFIC = {("vlong_1x32x32768x128", True): 1620613888 + 1022937088}
+_TRAFFIC = {("vlong_1x32x32768x128", True): 1622057728 + 1023449856}
 
 
 def _peaks():
@@ -112,39 +112,55 @@ class ClockSampler:
 # ------------------------------------------------------------------ our arm
 
 class Runner:
-    """Device buffers and the three C-ABI calls of one step."""
+    """Device buffers and the three C-ABI calls of one step (the general-mask entry
+    points: Q, dO have Nq rows per head, K, V have Nk; optional sliding window)."""
 
-    def __init__(self, fa, torch, w: si.Workload, causal: bool, dev):
-        self.fa, self.torch, self.w, self.causal = fa, torch, w, causal
-        Q, K, V, dO = si.make_workload(w)
+    def __init__(self, fa, torch, w: si.Workload, causal: bool, dev, Nq=None, Nk=None, window=0):
+        self.fa, self.torch, self.w, self.causal, self.window = fa, torch, w, causal, window
+        self.Nq, self.Nk = Nq or w.N, Nk or w.N
+        B, H, d = w.B, w.H, w.d
+        Q, K, V, dO = si.make_qkvdo(B, H, max(self.Nq, self.Nk), d, w.seed, w.qk_mult)
+        Q, dO = (t[:, :, :self.Nq].contiguous() for t in (Q, dO))
+        K, V = (t[:, :, :self.Nk].contiguous() for t in (K, V))
         self.host_in = [t.pin_memory() for t in (Q, K, V, dO)]
         self.q, self.k, self.v, self.do = (t.to(dev, non_blocking=False) for t in self.host_in)
-        B, H, N, d = w.B, w.H, w.N, w.d
         self.o = torch.empty_like(self.q)
-        self.lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        self.D = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        self.dq, self.dk, self.dv = (torch.empty_like(self.q) for _ in range(3))
-        self.ws_bytes = fa.fa_bwd_workspace_size(B, H, N, d, causal)
-        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.lse = torch.empty((B, H, self.Nq), dtype=torch.float32, device=dev)
+        self.D = torch.empty((B, H, self.Nq), dtype=torch.float32, device=dev)
+        self.dq = torch.empty_like(self.q)
+        self.dk, self.dv = torch.empty_like(self.k), torch.empty_like(self.v)
+        self.ws_bytes = fa.fa_bwd_workspace_size_ex(B, H, self.Nq, self.Nk, d, causal, window)
+        self.ws = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=dev)
         self.stream = torch.cuda.current_stream(dev)
         self.s = self.stream.cuda_stream
         self.scale = w.scale
 
     def fwd(self):
         w, fa = self.w, self.fa
-        fa.check(fa.fa_fwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(), self.o.data_ptr(),
-                           self.lse.data_ptr(), w.B, w.H, w.N, w.d, self.causal, self.scale, self.s), "fa_fwd")
+        fa.check(fa.fa_fwd_ex(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(), self.o.data_ptr(),
+                              self.lse.data_ptr(), w.B, w.H, self.Nq, self.Nk, w.d, self.causal, self.window, self.scale,
+                              self.s), "fa_fwd_ex")
 
     def bwd(self):
         w, fa = self.w, self.fa
-        fa.check(fa.fa_bwd_preprocess(self.o.data_ptr(), self.do.data_ptr(), self.D.data_ptr(), w.B, w.H, w.N, w.d,
-                                      self.s), "fa_bwd_preprocess")
-        fa.check(fa.fa_bwd(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(), self.o.data_ptr(),
-                           self.do.data_ptr(), self.lse.data_ptr(), self.D.data_ptr(), self.dq.data_ptr(),
-                           self.dk.data_ptr(), self.dv.data_ptr(), w.B, w.H, w.N, w.d, self.causal, self.scale,
-                           self.ws.data_ptr(), self.ws_bytes, self.s), "fa_bwd")
+        fa.check(fa.fa_bwd_preprocess(self.o.data_ptr(), self.do.data_ptr(), self.D.data_ptr(), w.B, w.H, self.Nq,
+                                      w.d, self.s), "fa_bwd_preprocess")
+        fa.check(fa.fa_bwd_ex(self.q.data_ptr(), self.k.data_ptr(), self.v.data_ptr(), self.o.data_ptr(),
+                              self.do.data_ptr(), self.lse.data_ptr(), self.D.data_ptr(), self.dq.data_ptr(),
+                              self.dk.data_ptr(), self.dv.data_ptr(), w.B, w.H, self.Nq, self.Nk, w.d, self.causal,
+                              self.window, self.scale, self.ws.data_ptr(), self.ws_bytes, self.s), "fa_bwd_ex")
+
+    def visible_pairs(self):
+        """(query, key) entries the mask leaves visible per head (the masked FLOP count is
+        4 d and 10 d times this), counted from the mask's definition."""
+        off = self.Nk - self.Nq
+        i = np.arange(self.Nq, dtype=np.int64)
+        hi = np.minimum(self.Nk - 1, i + off) if self.causal else np.full_like(i, self.Nk - 1)
+        lo = np.maximum(0, i + off - self.window + 1) if self.window > 0 else np.zeros_like(i)
+        return int((hi - lo + 1).sum())
 
     # kernels this library launches per step: fwd, preprocess, bwd main, dQ convert
+    # (or, with the two-kernel backward: fwd, preprocess, key-tile kernel, query-tile kernel)
     LAUNCHES_PER_STEP = 4
 
 
@@ -323,6 +339,39 @@ def per_config(fa, torch, dev, peaks):
             "fwd_bwd_tflops": round((ff + fb) / (fwd_ms + bwd_ms) / 1e9, 1),
             "ms_per_step": round((fwd_ms + bwd_ms) / 10, 4)}
         del r
+    # the general mask (FLOPs counted on the visible entries: 4 d and 10 d per entry)
+    for label, name, Nq, Nk, window in (
+            ("long_1x32x8192x128_causal_window1024", "long_1x32x8192x128", 8192, 8192, 1024),
+            ("prefill_1x32_2048q_32768k_x128_causal", "vlong_1x32x32768x128", 2048, 32768, 0)):
+        w = si.WORKLOADS[name]
+        r = Runner(fa, torch, w, True, dev, Nq=Nq, Nk=Nk, window=window)
+        fwd_ms, bwd_ms = time_steps(torch, r, 10, 3, flush=lambda: flush_buf.zero_())
+        vp = r.visible_pairs() * w.B * w.H
+        ff, fb = 4.0 * w.d * vp * 10, 10.0 * w.d * vp * 10
+        out[label] = {"fwd_tflops": round(ff / fwd_ms / 1e9, 1), "bwd_tflops": round(fb / bwd_ms / 1e9, 1),
+                      "fwd_bwd_tflops": round((ff + fb) / (fwd_ms + bwd_ms) / 1e9, 1),
+                      "ms_per_step": round((fwd_ms + bwd_ms) / 10, 4), "visible_pairs_per_head": vp // (w.B * w.H)}
+        del r
+    # decode (one new query per sequence against an 8192-key cache): forward only, HBM-bound
+    w = si.Workload("decode_16x32x1q_8192k_x128", 16, 32, 8192, 128, (True,), seed=5)
+    r = Runner(fa, torch, w, True, dev, Nq=1, Nk=8192)
+    for _ in range(3):
+        r.fwd()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    total = 0.0
+    for _ in range(10):
+        flush_buf.zero_()
+        ev[0].record(r.stream)
+        r.fwd()
+        ev[1].record(r.stream)
+        torch.cuda.synchronize()
+        total += ev[0].elapsed_time(ev[1])
+    ms = total / 10
+    bytes_ = w.B * w.H * (2 * 8192 * w.d * 2 + 2 * w.d * 2 + 4)  # K, V read; q read, o and L written
+    out["decode_16x32x1q_8192k_x128_fwd"] = {"ms": round(ms, 4), "gbs": round(bytes_ / ms / 1e6, 1),
+                                             "hbm_peak_gbs": float(peaks.get("hbm_gbs", 0.0)) or None}
+    del r
     return out
 
 

@@ -61,12 +61,15 @@ struct FwdCfg {
 // wait-site codes recorded in the status word
 enum : int { SITE_FWD_PRODUCER = 0x101, SITE_FWD_MMA = 0x102, SITE_FWD_SOFTMAX = 0x103 };
 
-template <int D, bool CAUSAL>
+// MASK: 0 none, 1 causal, 2 causal with a sliding window (compile-time, so that
+// the window's lower bound costs nothing in the other two).
+template <int D, int MASK>
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ Lout,
                int Nq, int Nk, int window, float c_log2, int* status, unsigned long long* tile_counter) {
   using C = FwdCfg<D>;
+  constexpr bool CAUSAL = MASK >= 1, WINDOW = MASK == 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const uint32_t sb = smem_u32(smem);
@@ -82,7 +85,7 @@ __global__ void __launch_bounds__(256, 1)
   const int off = Nk - Nq;  // position of query row i is i + off
   // visible key tiles jlo .. jlo + n_kv - 1 (whole-tile skip on both sides of the band)
   int jlo = 0, jhi = 0;
-  key_tile_range(qt, C::BM, C::BN, Nq, Nk, CAUSAL, window, &jlo, &jhi);
+  key_tile_range(qt, C::BM, C::BN, Nq, Nk, CAUSAL, WINDOW ? window : 0, &jlo, &jhi);
   const int n_kv = jhi - jlo + 1;
 
   if (threadIdx.x == 0) {
@@ -208,11 +211,11 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int k = 0; k < 128; ++k) s[k] = __uint_as_float(r[k]);
       const int k0 = (jlo + j) * C::BN;
-      if ((CAUSAL && k0 + C::BN - 1 > qt * C::BM + off) || (window > 0 && k0 <= qt * C::BM + C::BM - 1 + off - window) ||
+      if ((CAUSAL && k0 + C::BN - 1 > qt * C::BM + off) || (WINDOW && k0 <= qt * C::BM + C::BM - 1 + off - window) ||
           k0 + C::BN > Nk) {
         // this row sees tile columns lo .. hi (position q + off; keys below Nk)
         const int hi = min(CAUSAL ? q + off - k0 : C::BN - 1, Nk - 1 - k0);
-        const int lo = window > 0 ? q + off - window + 1 - k0 : 0;
+        const int lo = WINDOW ? q + off - window + 1 - k0 : 0;
 #pragma unroll
         for (int k = 0; k < 128; ++k)
           if (k > hi || k < lo) s[k] = -INFINITY;
@@ -252,7 +255,7 @@ __global__ void __launch_bounds__(256, 1)
       }
       // a row whose keys so far were all masked (a window's first tile) keeps
       // m = -inf; its P is 0 and the first visible tile rescales by 0
-      const float neg_m = m_run == -INFINITY ? 0.f : -m_run;
+      const float neg_m = (WINDOW && m_run == -INFINITY) ? 0.f : -m_run;
       float lsum0 = 0.f, lsum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
       uint32_t p[64];
 #pragma unroll
@@ -316,14 +319,14 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 fa_status launch_fwd_t(const FwdLaunch& a) {
   using C = FwdCfg<D>;
   CUtensorMap mQ, mK, mV;
   if (!encode_bf16_3d(&mQ, a.Q, D, a.Nq, a.BH, C::CE, C::BM) ||
       !encode_bf16_3d(&mK, a.K, D, a.Nk, a.BH, C::CE, C::BN) || !encode_bf16_3d(&mV, a.V, D, a.Nk, a.BH, C::CE, C::BN))
     return FA_ERR_CUDA;
-  auto kern = fwd_kernel<D, CAUSAL>;
+  auto kern = fwd_kernel<D, MASK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
   const dim3 grid((a.Nq + C::BM - 1) / C::BM, a.BH);
@@ -337,9 +340,12 @@ fa_status launch_fwd_t(const FwdLaunch& a) {
 
 fa_status launch_fwd(const FwdLaunch& a) {
   switch (a.d) {
-    case 32: return a.causal ? launch_fwd_t<32, true>(a) : launch_fwd_t<32, false>(a);
-    case 64: return a.causal ? launch_fwd_t<64, true>(a) : launch_fwd_t<64, false>(a);
-    case 128: return a.causal ? launch_fwd_t<128, true>(a) : launch_fwd_t<128, false>(a);
+#define FA_FWD_MASKS(D) \
+  (a.window > 0 ? launch_fwd_t<D, 2>(a) : a.causal ? launch_fwd_t<D, 1>(a) : launch_fwd_t<D, 0>(a))
+    case 32: return FA_FWD_MASKS(32);
+    case 64: return FA_FWD_MASKS(64);
+    case 128: return FA_FWD_MASKS(128);
+#undef FA_FWD_MASKS
     default: return FA_ERR_UNSUPPORTED;
   }
 }
