@@ -18,12 +18,14 @@
 // convert pass.
 //
 // Every UMMA is M = 128, N = 128 (narrower UMMAs do not reach the tensor pipe's
-// rate).  Tensor memory (512 columns): dK 128 | dV 128 | S^T region 128 | dP^T
-// region 128.  In the S^T region, query half h (64 queries) keeps its bf16 P^T in
-// columns 64h .. 64h+31 and its bf16 dS^T in 64h+32 .. 64h+63, overwriting only
-// its own S^T.  The UMMA issue order S, dP, dV, dK, dQ^T, S(next), ... keeps the
-// tensor pipe busy while the element-wise warps form P (during dP), dS (during
-// dV) and hand dQ to L2 (during the next S).
+// rate).  Tensor memory (512 columns): dK 128 | dV 128 | two 128-column regions
+// that take turns.  Step i keeps S^T in region i % 2; there query half h (64
+// queries) overwrites its own S^T with its bf16 P^T (columns 64h .. 64h+31) and
+// dS^T (64h+32 .. 64h+63), and once dV and dK have read those, dQ_i^T is formed
+// over the whole region.  dP^T of step i goes to region (i + 1) % 2, which held
+// dQ^T of step i-1.  The element-wise warps take all of dP^T into registers before
+// forming dS, so S^T of step i+1 is formed in that region while dS of step i is
+// computed and dK of step i accumulates.
 //
 // Warps: 0 TMA producer (its 32 lanes also stage L*log2 e and D of each query
 // tile in shared memory, two tiles ahead), 1 and 2 UMMA issuers (one thread
@@ -54,8 +56,10 @@ struct B128 {
   static constexpr int TILE = 128 * 128 * 2;    // one 128 x 128 bf16 tile (two 64-column chunks)
   // small region at the start of dynamic shared memory
   enum : int {
-    B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6, B_PREADY = 7, B_DSREADY = 9, B_DKDONE = 11,
-    B_DQFULL = 12, B_DQCONS = 13, B_FINAL = 14, B_ADONE = 15, NBAR = 16
+    B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6,
+    B_PREADY = 7,  // [step parity][sub-chunk]: the element-wise warps may be a step ahead of issuer B
+    B_DSREADY = 11, B_DKDONE = 13, B_DQFULL = 14, B_DQCONS = 15, B_DPCONS = 16, B_FINAL = 17, B_ADONE = 18,
+    NBAR = 19
   };
   static constexpr int OFF_BAR = 0;
   static constexpr int OFF_MISC = NBAR * 8;     // tensor-memory base, abort flag
@@ -67,7 +71,9 @@ struct B128 {
   static constexpr int T_DS = 6 * TILE;         // dS^T [128 keys][128 queries]
   static constexpr int TILES = 7 * TILE;        // 224 KiB
   static constexpr int SMEM = 232448;           // the per-block maximum
-  static constexpr int TM_DK = 0, TM_DV = 128, TM_S = 256, TM_DP = 384, TM_COLS = 512;
+  // Two 128-column regions take turns: step i keeps S^T, then P^T | dS^T, then dQ^T
+  // in region i % 2, and dP^T in region (i + 1) % 2.
+  static constexpr int TM_DK = 0, TM_DV = 128, TM_R = 256, TM_COLS = 512;
   // with a 1 KiB-aligned base the tiles start at 3 KiB and end exactly at the limit
   static_assert(SMALL <= 3072 && 3072 + TILES <= SMEM, "shared memory budget");
 };
@@ -117,8 +123,10 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     mbar_init(bar(C::B_DPFULL), 1);
     for (int c = 0; c < 2; ++c) {  // the two 32-query sub-chunks of each thread's 64 queries
       mbar_init(bar(C::B_PREADY + c), C::NCOMP);
+      mbar_init(bar(C::B_PREADY + 2 + c), C::NCOMP);
       mbar_init(bar(C::B_DSREADY + c), C::NCOMP);
     }
+    mbar_init(bar(C::B_DPCONS), C::NCOMP);
     mbar_init(bar(C::B_DKDONE), 1);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQCONS), C::NDQ);
@@ -143,7 +151,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
   const bool skip = *abort_flag != 0;
 
   if (warp < 4) {
-  // warpgroup 0 gives registers to the others; warps 2 and 3 have no role
+  // warpgroup 0 (producer and UMMA issuers) gives registers to the others
   regs_dec<72>();
   if (warp == 0 && !skip) {
     // ---------------------------------------------------------------- producer (whole warp)
@@ -197,20 +205,21 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     for (int it = 0; ok && it < n_it; ++it) {
       const int s = it & 1;
       const uint32_t qb = tb + C::T_Q + s * 2 * C::TILE, db = tb + C::T_DO + s * 2 * C::TILE;
+      const uint32_t rs = tmem + C::TM_R + 128 * s, rd = tmem + C::TM_R + 128 * (s ^ 1);
       if (!(ok = mbar_wait(bar(C::B_QFULL + s), (it >> 1) & 1, guard, SITE_MMA))) break;
-      // the S^T region held P^T and dS^T of the previous step until dV and dK read them
-      if (it > 0 && !(ok = mbar_wait(bar(C::B_DKDONE), (it - 1) & 1, guard, SITE_MMA))) break;
+      // region s held dP^T of the previous step: every element-wise thread has read it
+      if (it > 0 && !(ok = mbar_wait(bar(C::B_DPCONS), (it - 1) & 1, guard, SITE_MMA))) break;
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_ss(tmem + C::TM_S, sdesc_kmajor<128, 128>(kb, ks), sdesc_kmajor<128, 128>(qb, ks), idKK, ks > 0);
+        mma_ss(rs, sdesc_kmajor<128, 128>(kb, ks), sdesc_kmajor<128, 128>(qb, ks), idKK, ks > 0);
       mma_commit(bar(C::B_SFULL));
-      // the dP^T region held dQ^T of the previous step until it was read
+      // region s^1 ended the previous step holding its dQ^T: the drain warps have read it
       if (it > 0 && !(ok = mbar_wait(bar(C::B_DQCONS), (it - 1) & 1, guard, SITE_MMA))) break;
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_ss(tmem + C::TM_DP, sdesc_kmajor<128, 128>(vb, ks), sdesc_kmajor<128, 128>(db, ks), idKK, ks > 0);
+        mma_ss(rd, sdesc_kmajor<128, 128>(vb, ks), sdesc_kmajor<128, 128>(db, ks), idKK, ks > 0);
       mma_commit(bar(C::B_DPFULL));
     }
     mma_commit(bar(C::B_ADONE));  // drain point for teardown
@@ -226,18 +235,19 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
     for (int it = 0; it < n_it; ++it) {
       const int s = it & 1;
       const uint32_t qb = tb + C::T_Q + s * 2 * C::TILE, db = tb + C::T_DO + s * 2 * C::TILE;
+      const uint32_t rs = tmem + C::TM_R + 128 * s;
       // dV += P^T dO_i.  Query block ks (16 queries) is in half ks/4, sub-chunk (ks%4)/2;
       // its bf16 P^T sits in columns 64 (ks/4) + 8 (ks%4).  Sub-chunk 0 (blocks 0,1,4,5)
       // is ready before sub-chunk 1 (blocks 2,3,6,7).
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        if (!(ok = mbar_wait(bar(C::B_PREADY + c), it & 1, guard, SITE_MMA))) break;
+        if (!(ok = mbar_wait(bar(C::B_PREADY + 2 * s + c), (it >> 1) & 1, guard, SITE_MMA))) break;
         tc_fence_after();
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int ks = 4 * (u >> 1) + 2 * c + (u & 1);
-          mma_ts(tmem + C::TM_DV, tmem + C::TM_S + 64 * (ks >> 2) + (ks & 3) * 8, sdesc_mnmajor<128, 128>(db, ks),
-                 idTN, (it > 0 || ks > 0));
+          mma_ts(tmem + C::TM_DV, rs + 64 * (ks >> 2) + (ks & 3) * 8, sdesc_mnmajor<128, 128>(db, ks), idTN,
+                 (it > 0 || ks > 0));
         }
       }
       if (!ok) break;
@@ -249,17 +259,20 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int ks = 4 * (u >> 1) + 2 * c + (u & 1);
-          mma_ts(tmem + C::TM_DK, tmem + C::TM_S + 64 * (ks >> 2) + 32 + (ks & 3) * 8,
-                 sdesc_mnmajor<128, 128>(qb, ks), idTN, (it > 0 || ks > 0));
+          mma_ts(tmem + C::TM_DK, rs + 64 * (ks >> 2) + 32 + (ks & 3) * 8, sdesc_mnmajor<128, 128>(qb, ks), idTN,
+                 (it > 0 || ks > 0));
         }
       }
       if (!ok) break;
       mma_commit(bar(C::B_DKDONE));
       mma_commit(bar(C::B_QEMPTY + s));  // Q_i, dO_i have no later reader
-      // dQ_i^T = K^T dS^T over the dP^T columns (the element-wise warps have read dP^T)
+      // dQ_i^T = K^T dS^T (both from shared memory) over region s, once dV and dK have
+      // read its P^T and dS^T
+      if (!(ok = mbar_wait(bar(C::B_DKDONE), it & 1, guard, SITE_MMA))) break;
+      tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        mma_ss(tmem + C::TM_DP, sdesc_mnmajor<128, 128>(kb, ks), sdesc_mnmajor<128, 128>(dsb, ks), idMN, ks > 0);
+        mma_ss(rs, sdesc_mnmajor<128, 128>(kb, ks), sdesc_mnmajor<128, 128>(dsb, ks), idMN, ks > 0);
       mma_commit(bar(C::B_DQFULL));
     }
     mma_commit(bar(C::B_FINAL));
@@ -278,7 +291,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       tc_fence_after();
       uint32_t r[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tl + C::TM_DP + 32 * c, r + 32 * c);
+      for (int c = 0; c < 4; ++c) tmem_ld32(tl + C::TM_R + 128 * (j & 1) + 32 * c, r + 32 * c);
       tmem_ld_wait<128>(r);
       tc_fence_before();
       mbar_arrive(bar(C::B_DQCONS));
@@ -311,6 +324,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       if (!(ok = mbar_wait_warp(bar(C::B_QFULL + s), (it >> 1) & 1, guard, SITE_COMPUTE))) break;
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL), it & 1, guard, SITE_COMPUTE))) break;
       tc_fence_after();
+      const uint32_t rs = tl + C::TM_R + 128 * s, rd = tl + C::TM_R + 128 * (s ^ 1);
       const int qh = (i0 + it) * C::BM + 64 * h;  // first query of this half
       const float4* L4 = reinterpret_cast<const float4*>(smem_raw + C::OFF_LD + s * C::LD_BYTES) + 16 * h;
       const float4* D4 = L4 + C::BM / 4;
@@ -327,7 +341,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t r[32];
-        tmem_ld32(tl + C::TM_S + 64 * h + 32 * c, r);
+        tmem_ld32(rs + 64 * h + 32 * c, r);
         tmem_ld_wait<32>(r);
         auto body = [&](auto mask_tag) {
           constexpr bool MASK = decltype(mask_tag)::value;
@@ -355,20 +369,27 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
           }
         };
         if (masked) body(std::true_type{}); else body(std::false_type{});
-        tmem_st16(tl + C::TM_S + 64 * h + 16 * c, pk + 16 * c);
+        tmem_st16(rs + 64 * h + 16 * c, pk + 16 * c);
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(C::B_PREADY + c));
+        mbar_arrive(bar(C::B_PREADY + 2 * s + c));
       }
       // ---- dS^T = P^T (dP^T - D), from the same bf16 P that enters dV; two sub-chunks
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), it & 1, guard, SITE_COMPUTE))) break;
       tc_fence_after();
       uint8_t* row = tiles + C::T_DS + h * (128 * 128) + kr * 128;
+      // all of this thread's dP^T out of tensor memory first, so that S^T of the next
+      // step can be formed in its region while dS is computed
+      uint32_t rdp[64];
+      tmem_ld32(rd + 64 * h, rdp);
+      tmem_ld32(rd + 64 * h + 32, rdp + 32);
+      tmem_ld_wait<64>(rdp);
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DPCONS));
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        uint32_t r[32], dk[16];
-        tmem_ld32(tl + C::TM_DP + 64 * h + 32 * c, r);
-        tmem_ld_wait<32>(r);
+        const uint32_t* r = rdp + 32 * c;
+        uint32_t dk[16];
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const float4 dd = D4[8 * c + v];
@@ -384,7 +405,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
             dk[x >> 1] = pack_bf16x2(d0, d1);
           }
         }
-        tmem_st16(tl + C::TM_S + 64 * h + 32 + 16 * c, dk);
+        tmem_st16(rs + 64 * h + 32 + 16 * c, dk);
         // dS^T row kr, queries 64h + 32c .. +31: four 16-byte units of the swizzled row
 #pragma unroll
         for (int u = 0; u < 4; ++u)
