@@ -4,14 +4,14 @@
 // both).  No atomics and no workspace: each output is written once.
 //
 // bwd_kv_kernel: one CTA per 128 keys (keys on the 128 tensor-memory lanes),
-//   S^T = K Q_i^T, dP^T = V dO_i^T (UMMA), P^T, dS^T (8 element-wise warps, in two
-//   32-query sub-chunks), dV += P^T dO_i, dK += dS^T Q_i (UMMA, A from tensor
+//   S^T = K Q_i^T, dP^T = V dO_i^T (UMMA), P^T, dS^T (16 element-wise warps, 32
+//   queries each), dV += P^T dO_i, dK += dS^T Q_i (UMMA, A from tensor
 //   memory).  Tensor memory: dK | dV | two regions that take turns holding S^T
 //   (then P^T | dS^T) and dP^T.
 // bwd_q_kernel: one CTA per 128 queries (queries on the lanes; L and D of the
 //   row kept in registers), S = Q K_j^T (two buffers), dP = dO V_j^T (UMMA),
-//   P = 2^(S c - L log2 e), dS = P (dP - D) (8 warps, two per lane quarter, one
-//   per 64-key half), dQ += dS K_j (UMMA, A = dS in tensor memory), then
+//   P = 2^(S c - L log2 e), dS = P (dP - D) (16 warps, four per lane quarter, one
+//   per 32-key quarter), dQ += dS K_j (UMMA, A = dS in tensor memory), then
 //   dQ * scale -> bf16.  Tensor memory: S x2 | dP | dQ.
 // Both kernels split UMMA issue over two threads, as the other kernels do.
 #include <type_traits>
@@ -30,7 +30,7 @@ enum : int { SITE_KV = 0x221, SITE_Q = 0x222 };
 
 // ============================================================================ dK, dV
 struct KVC {
-  static constexpr int NTHREADS = 384, NCOMP = 256;
+  static constexpr int NTHREADS = 640, NCOMP = 512;  // 4 + 16 element-wise warps
   enum : int {
     B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6,
     B_PREADY = 7,  // [step parity][sub-chunk]: the element-wise warps may be a step ahead of issuer B
@@ -75,9 +75,10 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(C::B_QFULL + s), 1 + 32);
       mbar_init(bar(C::B_QEMPTY + s), 1);
-      mbar_init(bar(C::B_PREADY + 2 * s), C::NCOMP);
-      mbar_init(bar(C::B_PREADY + 2 * s + 1), C::NCOMP);
-      mbar_init(bar(C::B_DSREADY + s), C::NCOMP);
+      // sub-chunk c = query quarters c and 2 + c: half of the element-wise threads
+      mbar_init(bar(C::B_PREADY + 2 * s), C::NCOMP / 2);
+      mbar_init(bar(C::B_PREADY + 2 * s + 1), C::NCOMP / 2);
+      mbar_init(bar(C::B_DSREADY + s), C::NCOMP / 2);
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
@@ -179,7 +180,8 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int ks = 4 * (u >> 1) + 2 * c + (u & 1);
-          mma_ts(tmem + C::TM_DV, rs + 64 * (ks >> 2) + (ks & 3) * 8, sdesc_mnmajor<128, 128>(db, ks), idTN,
+          // query block ks (16 queries) is in quarter ks/2: P^T at 32 (ks/2) + 8 (ks%2)
+          mma_ts(tmem + C::TM_DV, rs + 32 * (ks >> 1) + 8 * (ks & 1), sdesc_mnmajor<128, 128>(db, ks), idTN,
                  (it > 0 || ks > 0));
         }
       }
@@ -191,7 +193,7 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int ks = 4 * (u >> 1) + 2 * c + (u & 1);
-          mma_ts(tmem + C::TM_DK, rs + 64 * (ks >> 2) + 32 + (ks & 3) * 8, sdesc_mnmajor<128, 128>(qb, ks), idTN,
+          mma_ts(tmem + C::TM_DK, rs + 32 * (ks >> 1) + 16 + 8 * (ks & 1), sdesc_mnmajor<128, 128>(qb, ks), idTN,
                  (it > 0 || ks > 0));
         }
       }
@@ -202,7 +204,9 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
     mma_commit(bar(C::B_FINAL));
   } else if (warp >= 4 && !skip) {
     // ---------------------------------------------------------------- element-wise warps
-    const int qw = warp & 3, h = (warp - 4) >> 2, kr = qw * 32 + lane, key = kt * 128 + kr;
+    // warp w: tensor-memory lane quarter w % 4 (32 keys), query quarter (w - 4) / 4
+    // (32 queries); P^T and dS^T of a query quarter go over its own 32 S^T columns
+    const int qw = warp & 3, qq = (warp - 4) >> 2, c = qq & 1, kr = qw * 32 + lane, key = kt * 128 + kr;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
     const uint64_t cc = f2pack(c_log2, c_log2);
     bool ok = true;
@@ -211,26 +215,25 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
       if (!(ok = mbar_wait_warp(bar(C::B_QFULL + s), (it >> 1) & 1, guard, SITE_KV))) break;
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL), it & 1, guard, SITE_KV))) break;
       tc_fence_after();
-      const uint32_t rs = tl + C::TM_R + 128 * s, rd = tl + C::TM_R + 128 * (s ^ 1);
-      const int qh = (i0 + it) * 128 + 64 * h;
-      const float4* L4 = reinterpret_cast<const float4*>(smem_raw + C::OFF_LD + s * C::LD_BYTES) + 16 * h;
+      const uint32_t rs = tl + C::TM_R + 128 * s + 32 * qq, rd = tl + C::TM_R + 128 * (s ^ 1) + 32 * qq;
+      const int q0 = (i0 + it) * 128 + 32 * qq;  // first query of this quarter
+      const float4* L4 = reinterpret_cast<const float4*>(smem_raw + C::OFF_LD + s * C::LD_BYTES) + 8 * qq;
       const float4* D4 = L4 + 32;
-      const bool masked = (CAUSAL && kt * 128 + 127 > qh + off) || (window > 0 && kt * 128 <= qh + 63 + off - window) ||
+      const bool masked = (CAUSAL && kt * 128 + 127 > q0 + off) || (window > 0 && kt * 128 <= q0 + 31 + off - window) ||
                           (kt * 128 + 128 > Nk);
-      // queries of this half (0..63) that see this thread's key
-      const int qlo = CAUSAL ? key - off - qh : 0;
-      const int qhi = key >= Nk ? -1 : (window > 0 ? key - off + window - 1 - qh : 63);
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      // queries of this quarter (0..31) that see this thread's key
+      const int qlo = CAUSAL ? key - off - q0 : 0;
+      const int qhi = key >= Nk ? -1 : (window > 0 ? key - off + window - 1 - q0 : 31);
+      uint32_t pk[16];
+      {
         uint32_t r[32];
-        tmem_ld32(rs + 64 * h + 32 * c, r);
+        tmem_ld32(rs, r);
         tmem_ld_wait<32>(r);
         auto body = [&](auto mask_tag) {
           constexpr bool MASK = decltype(mask_tag)::value;
 #pragma unroll
           for (int v = 0; v < 8; ++v) {
-            const float4 l = L4[8 * c + v];
+            const float4 l = L4[v];
             float p[4];
 #pragma unroll
             for (int y = 0; y < 4; y += 2) {
@@ -241,56 +244,50 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
                        t0, t1);
               p[y] = ex2(t0);
               p[y + 1] = ex2(t1);
-              if (MASK) {
-                const int xs = 32 * c + x;  // query of the half: visible iff qlo <= xs <= qhi
-                if (xs < qlo || xs > qhi) p[y] = 0.f;
-                if (xs + 1 < qlo || xs + 1 > qhi) p[y + 1] = 0.f;
+              if (MASK) {  // visible iff qlo <= x <= qhi
+                if (x < qlo || x > qhi) p[y] = 0.f;
+                if (x + 1 < qlo || x + 1 > qhi) p[y + 1] = 0.f;
               }
             }
-            pk[16 * c + 2 * v] = pack_bf16x2(p[0], p[1]);
-            pk[16 * c + 2 * v + 1] = pack_bf16x2(p[2], p[3]);
+            pk[2 * v] = pack_bf16x2(p[0], p[1]);
+            pk[2 * v + 1] = pack_bf16x2(p[2], p[3]);
           }
         };
         if (masked) body(std::true_type{}); else body(std::false_type{});
-        tmem_st16(rs + 64 * h + 16 * c, pk + 16 * c);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_PREADY + 2 * s + c));
       }
+      tmem_st16(rs, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_PREADY + 2 * s + c));
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), it & 1, guard, SITE_KV))) break;
       tc_fence_after();
-      // take all of this thread's dP^T out of tensor memory first, so that S^T of the
-      // next step can be formed in its region while dS is computed
-      uint32_t rdp[64];
-      tmem_ld32(rd + 64 * h, rdp);
-      tmem_ld32(rd + 64 * h + 32, rdp + 32);
-      tmem_ld_wait<64>(rdp);
+      // this thread's dP^T out of tensor memory first, so that S^T of the next step
+      // can be formed in its region while dS is computed
+      uint32_t r[32];
+      tmem_ld32(rd, r);
+      tmem_ld_wait<32>(r);
       tc_fence_before();
       mbar_arrive(bar(C::B_DPCONS));
+      uint32_t dk[16];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t* r = rdp + 32 * c;
-        uint32_t dk[16];
+      for (int v = 0; v < 8; ++v) {
+        const float4 dd = D4[v];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const float4 dd = D4[8 * c + v];
-#pragma unroll
-          for (int y = 0; y < 4; y += 2) {
-            const int x = 4 * v + y;
-            const uint32_t w = pk[16 * c + (x >> 1)];
-            float d0, d1;
-            f2unpack(fmul2(f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
-                           fadd2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])),
-                                 y == 0 ? f2pack(-dd.x, -dd.y) : f2pack(-dd.z, -dd.w))),
-                     d0, d1);
-            dk[x >> 1] = pack_bf16x2(d0, d1);
-          }
+        for (int y = 0; y < 4; y += 2) {
+          const int x = 4 * v + y;
+          const uint32_t w = pk[x >> 1];
+          float d0, d1;
+          f2unpack(fmul2(f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
+                         fadd2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])),
+                               y == 0 ? f2pack(-dd.x, -dd.y) : f2pack(-dd.z, -dd.w))),
+                   d0, d1);
+          dk[x >> 1] = pack_bf16x2(d0, d1);
         }
-        tmem_st16(rs + 64 * h + 32 + 16 * c, dk);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_DSREADY + c));
       }
+      tmem_st16(rs + 16, dk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DSREADY + c));
     }
     if (ok) ok = mbar_wait_warp(bar(C::B_FINAL), 0, guard, SITE_KV);
     if (ok) {
@@ -298,25 +295,22 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const float f = t == 0 ? scale : 1.f;
-        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (krow0 + key) * 128 + 64 * h;
+        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (krow0 + key) * 128 + 32 * qq;
+        uint32_t r[32];
+        tmem_ld32(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 32 * qq, r);
+        tmem_ld_wait<32>(r);
+        if (n_it == 0) {  // no query sees these keys: the accumulators were never written
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 64 * h + 32 * c, r);
-          tmem_ld_wait<32>(r);
-          if (n_it == 0) {  // no query sees these keys: the accumulators were never written
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (key < Nk) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-          }
-          if (key < Nk) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * f, __uint_as_float(r[8 * i + 1]) * f),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 2]) * f, __uint_as_float(r[8 * i + 3]) * f),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 4]) * f, __uint_as_float(r[8 * i + 5]) * f),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 6]) * f, __uint_as_float(r[8 * i + 7]) * f));
-          }
+          for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * f, __uint_as_float(r[8 * i + 1]) * f),
+                               pack_bf16x2(__uint_as_float(r[8 * i + 2]) * f, __uint_as_float(r[8 * i + 3]) * f),
+                               pack_bf16x2(__uint_as_float(r[8 * i + 4]) * f, __uint_as_float(r[8 * i + 5]) * f),
+                               pack_bf16x2(__uint_as_float(r[8 * i + 6]) * f, __uint_as_float(r[8 * i + 7]) * f));
         }
       }
     }
@@ -338,7 +332,7 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
 
 // ============================================================================ dQ
 struct QC {
-  static constexpr int NTHREADS = 384, NCOMP = 256;
+  static constexpr int NTHREADS = 640, NCOMP = 512;  // 4 + 16 element-wise warps
   // K_j lives until dQ_j is done, V_j only until dP_j is: three K stages and two
   // V stages let each load start two steps ahead of its use.
   static constexpr int KST = 3, VST = 2;
@@ -390,7 +384,8 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
       mbar_init(bar(C::B_VEMPTY + b), 1);
       mbar_init(bar(C::B_SFULL + b), 1);
       mbar_init(bar(C::B_SFREE + b), 1);
-      for (int c = 0; c < 2; ++c) mbar_init(bar(C::B_DSREADY + 2 * b + c), C::NCOMP);
+      // sub-chunk c = key quarters c and 2 + c: half of the element-wise threads
+      for (int c = 0; c < 2; ++c) mbar_init(bar(C::B_DSREADY + 2 * b + c), C::NCOMP / 2);
     }
     mbar_init(bar(C::B_DPFULL), 1);
     mbar_init(bar(C::B_DPCONS), C::NCOMP);
@@ -475,8 +470,8 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int ks = 4 * (u >> 1) + 2 * c + (u & 1);  // key block: half ks/4, sub-chunk (ks%4)/2
-          mma_ts(tmem + C::TM_DQ, tmem + C::TM_S + 128 * s + 64 * (ks >> 2) + (ks & 3) * 8,
+          const int ks = 4 * (u >> 1) + 2 * c + (u & 1);  // key block ks: quarter ks/2, dS at 32 (ks/2) + 8 (ks%2)
+          mma_ts(tmem + C::TM_DQ, tmem + C::TM_S + 128 * s + 32 * (ks >> 1) + 8 * (ks & 1),
                  sdesc_mnmajor<128, 128>(kb, ks), idTN, (j > 0 || ks > 0));
         }
       }
@@ -487,7 +482,9 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
     mma_commit(bar(C::B_FINAL));
   } else if (warp >= 4 && !skip) {
     // ---------------------------------------------------------------- element-wise warps
-    const int qw = warp & 3, h = (warp - 4) >> 2, row = qw * 32 + lane, q = qt * 128 + row;
+    // warp w: tensor-memory lane quarter w % 4 (32 query rows), key quarter (w - 4) / 4
+    // (32 keys); the bf16 dS of a key quarter goes over its own 32 S columns
+    const int qw = warp & 3, kq = (warp - 4) >> 2, c = kq & 1, row = qw * 32 + lane, q = qt * 128 + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(qw * 32) << 16);
     const float nl = q < Nq ? -Lg[row0 + q] * kLog2e : -INFINITY;  // rows past Nq: P = 0
     const float dq = q < Nq ? Dg[row0 + q] : 0.f;
@@ -498,17 +495,17 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
       const int s = j & 1;
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL + s), (j >> 1) & 1, guard, SITE_Q))) break;
       tc_fence_after();
-      const int kh = (jlo + j) * 128 + 64 * h;  // first key of this half
-      const bool masked = (CAUSAL && kh + 63 > qt * 128 + off) || (window > 0 && kh <= qt * 128 + 127 + off - window) ||
-                          (kh + 64 > Nk);
-      // keys of this half (0..63) this row sees: position p, keys below Nk
-      const int khi = min(CAUSAL ? p - kh : 63, Nk - 1 - kh);
-      const int klo = window > 0 ? p - window + 1 - kh : 0;
-      uint32_t pk[32];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      const int k0 = (jlo + j) * 128 + 32 * kq;  // first key of this quarter
+      const bool masked = (CAUSAL && k0 + 31 > qt * 128 + off) || (window > 0 && k0 <= qt * 128 + 127 + off - window) ||
+                          (k0 + 32 > Nk);
+      // keys of this quarter (0..31) this row sees: position p, keys below Nk
+      const int khi = min(CAUSAL ? p - k0 : 31, Nk - 1 - k0);
+      const int klo = window > 0 ? p - window + 1 - k0 : 0;
+      const uint32_t sc = tl + C::TM_S + 128 * s + 32 * kq;
+      uint32_t pk[16];
+      {
         uint32_t r[32];
-        tmem_ld32(tl + C::TM_S + 128 * s + 64 * h + 32 * c, r);
+        tmem_ld32(sc, r);
         tmem_ld_wait<32>(r);
         auto body = [&](auto mask_tag) {
           constexpr bool MASK = decltype(mask_tag)::value;
@@ -517,62 +514,51 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
             float t0, t1;
             f2unpack(ffma2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), cc, nl2), t0, t1);
             float p0 = ex2(t0), p1 = ex2(t1);
-            if (MASK) {
-              const int xs = 32 * c + x;  // key of the half: visible iff klo <= xs <= khi
-              if (xs < klo || xs > khi) p0 = 0.f;
-              if (xs + 1 < klo || xs + 1 > khi) p1 = 0.f;
+            if (MASK) {  // visible iff klo <= x <= khi
+              if (x < klo || x > khi) p0 = 0.f;
+              if (x + 1 < klo || x + 1 > khi) p1 = 0.f;
             }
-            pk[16 * c + (x >> 1)] = pack_bf16x2(p0, p1);
+            pk[x >> 1] = pack_bf16x2(p0, p1);
           }
         };
         if (masked) body(std::true_type{}); else body(std::false_type{});
       }
       if (!(ok = mbar_wait_warp(bar(C::B_DPFULL), j & 1, guard, SITE_Q))) break;
       tc_fence_after();
-      uint32_t rdp[64];
-      tmem_ld32(tl + C::TM_DP + 64 * h, rdp);
-      tmem_ld32(tl + C::TM_DP + 64 * h + 32, rdp + 32);
-      tmem_ld_wait<64>(rdp);
+      uint32_t r[32];
+      tmem_ld32(tl + C::TM_DP + 32 * kq, r);
+      tmem_ld_wait<32>(r);
       tc_fence_before();
       mbar_arrive(bar(C::B_DPCONS));
+      uint32_t dk[16];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t* r = rdp + 32 * c;
-        uint32_t dk[16];
-#pragma unroll
-        for (int x = 0; x < 32; x += 2) {
-          const uint32_t w = pk[16 * c + (x >> 1)];
-          float d0, d1;
-          f2unpack(fmul2(f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
-                         fadd2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), nd2)),
-                   d0, d1);
-          dk[x >> 1] = pack_bf16x2(d0, d1);
-        }
-        // dS of keys kh + 32c .. +31 over S columns this half has already read
-        tmem_st16(tl + C::TM_S + 128 * s + 64 * h + 16 * c, dk);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(bar(C::B_DSREADY + 2 * s + c));
+      for (int x = 0; x < 32; x += 2) {
+        const uint32_t w = pk[x >> 1];
+        float d0, d1;
+        f2unpack(fmul2(f2pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u)),
+                       fadd2(f2pack(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), nd2)),
+                 d0, d1);
+        dk[x >> 1] = pack_bf16x2(d0, d1);
       }
+      tmem_st16(sc, dk);  // over this quarter's own S columns, already read
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DSREADY + 2 * s + c));
     }
     if (ok) ok = mbar_wait_warp(bar(C::B_FINAL), 0, guard, SITE_Q);
     if (ok) {
       tc_fence_after();
-      __nv_bfloat16* dst = dQ + (row0 + q) * 128 + 64 * h;
+      uint32_t r[32];
+      tmem_ld32(tl + C::TM_DQ + 32 * kq, r);
+      tmem_ld_wait<32>(r);
+      if (q < Nq) {
+        uint4* d4 = reinterpret_cast<uint4*>(dQ + (row0 + q) * 128 + 32 * kq);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tl + C::TM_DQ + 64 * h + 32 * c, r);
-        tmem_ld_wait<32>(r);
-        if (q < Nq) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * scale, __uint_as_float(r[8 * i + 1]) * scale),
-                               pack_bf16x2(__uint_as_float(r[8 * i + 2]) * scale, __uint_as_float(r[8 * i + 3]) * scale),
-                               pack_bf16x2(__uint_as_float(r[8 * i + 4]) * scale, __uint_as_float(r[8 * i + 5]) * scale),
-                               pack_bf16x2(__uint_as_float(r[8 * i + 6]) * scale, __uint_as_float(r[8 * i + 7]) * scale));
-        }
+        for (int i = 0; i < 4; ++i)
+          d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * scale, __uint_as_float(r[8 * i + 1]) * scale),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 2]) * scale, __uint_as_float(r[8 * i + 3]) * scale),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 4]) * scale, __uint_as_float(r[8 * i + 5]) * scale),
+                             pack_bf16x2(__uint_as_float(r[8 * i + 6]) * scale, __uint_as_float(r[8 * i + 7]) * scale));
       }
     }
   }
