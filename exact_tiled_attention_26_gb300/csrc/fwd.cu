@@ -220,9 +220,16 @@ __global__ void __launch_bounds__(256, 1)
         for (int k = 0; k < 128; ++k)
           if (k > hi || k < lo) s[k] = -INFINITY;
       }
-      float mx = s[0];
+      // row max as eight independent chains of 3-input maxes (depth ~10, not 127)
+      float m8[8];
 #pragma unroll
-      for (int k = 1; k < 128; ++k) mx = fmaxf(mx, s[k]);
+      for (int a = 0; a < 8; ++a) {
+        m8[a] = fmax3(s[16 * a], s[16 * a + 1], s[16 * a + 2]);
+#pragma unroll
+        for (int b = 3; b < 15; b += 2) m8[a] = fmax3(m8[a], s[16 * a + b], s[16 * a + b + 1]);
+        m8[a] = fmaxf(m8[a], s[16 * a + 15]);
+      }
+      const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
       const float m_tile = mx * c_log2;
       if (j == 0) {
         m_run = m_tile;
