@@ -263,21 +263,26 @@ __global__ void __launch_bounds__(256, 1)
       // a row whose keys so far were all masked (a window's first tile) keeps
       // m = -inf; its P is 0 and the first visible tile rescales by 0
       const float neg_m = (WINDOW && m_run == -INFINITY) ? 0.f : -m_run;
-      float lsum0 = 0.f, lsum1 = 0.f, rsum0 = 0.f, rsum1 = 0.f;
+      // two columns per packed f32x2 instruction: exponent argument, running sums of
+      // P (for L) and of P as rounded to bf16 (for O's normaliser); two chains each
+      const uint64_t cc2 = f2pack(c_log2, c_log2), nm2 = f2pack(neg_m, neg_m);
+      uint64_t ls[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)}, rs[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
       uint32_t p[64];
 #pragma unroll
       for (int k = 0; k < 128; k += 2) {
-        const float p0 = ex2(fmaf(s[k], c_log2, neg_m));
-        const float p1 = ex2(fmaf(s[k + 1], c_log2, neg_m));
-        lsum0 += p0;
-        lsum1 += p1;
+        float t0, t1;
+        f2unpack(ffma2(f2pack(s[k], s[k + 1]), cc2, nm2), t0, t1);
+        const float p0 = ex2(t0), p1 = ex2(t1);
+        ls[(k >> 1) & 1] = fadd2(ls[(k >> 1) & 1], f2pack(p0, p1));
         const uint32_t pk = pack_bf16x2(p0, p1);
         p[k >> 1] = pk;
-        rsum0 += __uint_as_float(pk << 16);
-        rsum1 += __uint_as_float(pk & 0xffff0000u);
+        rs[(k >> 1) & 1] = fadd2(rs[(k >> 1) & 1], f2pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
       }
-      l_run += lsum0 + lsum1;
-      lr_run += rsum0 + rsum1;
+      float a0, a1, a2, a3;
+      f2unpack(fadd2(ls[0], ls[1]), a0, a1);
+      f2unpack(fadd2(rs[0], rs[1]), a2, a3);
+      l_run += a0 + a1;
+      lr_run += a2 + a3;
       tmem_st32(tl + C::TM_S0 + b * 128, p);
       tmem_st32(tl + C::TM_S0 + b * 128 + 32, p + 32);
       tmem_st_wait();
