@@ -19,8 +19,9 @@ constexpr int kMaxDevices = 64;
 int* g_status_ptr[kMaxDevices] = {nullptr};
 std::mutex g_mu;
 unsigned long long* g_tile_counter = nullptr;
-int g_bwd_split = 0;                    // 0: the default below
+int g_bwd_split = 0;                    // 0: the defaults below
 constexpr int kDefaultBwdSplitD128 = 1;  // chosen by measurement on GB300
+constexpr int kDefaultBwdSplitD64 = 2;  // two kernels: faster at d = 64 (measured)
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -222,8 +223,9 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int 
 // Which backward form runs: 1 = one kernel over key tiles with dQ reduced in
 // the fp32 workspace, 2 = two kernels (key tiles for dK, dV; query tiles for dQ).
 static int bwd_split(int d) {
-  if (d != 128) return 1;
-  return g_bwd_split != 0 ? g_bwd_split : kDefaultBwdSplitD128;
+  if (d != 128 && d != 64) return 1;
+  if (g_bwd_split != 0) return g_bwd_split;
+  return d == 128 ? kDefaultBwdSplitD128 : kDefaultBwdSplitD64;
 }
 
 size_t fa_bwd_workspace_size_ex(int B, int H, int Nq, int Nk, int d, int causal, int window) {
@@ -271,7 +273,7 @@ fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, 
   if (status == nullptr) return FA_ERR_CUDA;
   BwdLaunch a{Q,  K,  V,  dO, L,      D,     static_cast<float*>(workspace), dK,     dV,
               B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
-  if (bwd_split(d) == 2) return launch_bwd_two_kernel_d128(a, dQ);
+  if (bwd_split(d) == 2) return launch_bwd_two_kernel(a, dQ);
   if (cudaMemsetAsync(workspace, 0, need, stream) != cudaSuccess) return FA_ERR_CUDA;
   st = launch_bwd(a);
   if (st != FA_OK) return st;

@@ -23,13 +23,14 @@ namespace fa {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int TILE = 128 * 128 * 2;  // one 128 x 128 bf16 tile (two 64-column chunks)
 constexpr int SMEM_MAX = 232448;
 
 enum : int { SITE_KV = 0x221, SITE_Q = 0x222 };
 
 // ============================================================================ dK, dV
+template <int D>
 struct KVC {
+  static constexpr int TD = 128 * D * 2, NCH = D / 64;  // a 128 x D bf16 tile, in 64-column chunks
   static constexpr int NTHREADS = 640, NCOMP = 512;  // 4 + 16 element-wise warps
   enum : int {
     B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6,
@@ -38,23 +39,23 @@ struct KVC {
   };
   static constexpr int OFF_MISC = NBAR * 8, OFF_LD = 256, LD_BYTES = 2 * 128 * 4;
   static constexpr int SMALL = OFF_LD + 2 * LD_BYTES;
-  static constexpr int T_K = 0, T_V = TILE, T_Q = 2 * TILE, T_DO = 3 * TILE;  // Q, dO: + s * 2 TILE
-  static constexpr int TILES = 6 * TILE;
+  static constexpr int T_K = 0, T_V = TD, T_Q = 2 * TD, T_DO = 3 * TD;  // Q, dO: + s * 2 TD
+  static constexpr int TILES = 6 * TD;
   static constexpr int SMEM = SMALL + 1024 + TILES;
   // Two 128-column regions alternate: step i keeps S^T (then P^T | dS^T) in region
   // i % 2 and dP^T in region (i + 1) % 2, so S^T of step i+1 can be formed as soon
   // as dP^T of step i has been read, while dK of step i is still being accumulated.
-  static constexpr int TM_DK = 0, TM_DV = 128, TM_R = 256;
+  static constexpr int TM_DK = 0, TM_DV = 128, TM_R = 256;  // dK, dV use D columns each
 };
 
-template <bool CAUSAL>
-__global__ void __launch_bounds__(KVC::NTHREADS, 1)
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(KVC<D>::NTHREADS, 1)
     bwd_kv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const float* __restrict__ Lg, const float* __restrict__ Dg, __nv_bfloat16* __restrict__ dK,
                   __nv_bfloat16* __restrict__ dV, int Nq, int Nk, int window, float c_log2, float scale, int* status,
                   unsigned long long* tile_counter) {
-  using C = KVC;
+  using C = KVC<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw + C::SMALL);
   const uint32_t sb = smem_u32(smem_raw), tb = smem_u32(tiles);
@@ -101,8 +102,8 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
   if (warp == 0 && !skip) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      mbar_expect_tx(bar(C::B_KV), 2 * TILE);
-      for (int c = 0; c < 2; ++c) {
+      mbar_expect_tx(bar(C::B_KV), 2 * C::TD);
+      for (int c = 0; c < C::NCH; ++c) {
         tma_load_3d(tb + C::T_K + c * 128 * 128, &tmK, bar(C::B_KV), c * 64, kt * 128, bh);
         tma_load_3d(tb + C::T_V + c * 128 * 128, &tmV, bar(C::B_KV), c * 64, kt * 128, bh);
       }
@@ -119,10 +120,10 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
       }
       if (!mbar_wait_warp(bar(C::B_QEMPTY + s), ((it >> 1) & 1) ^ 1, guard, SITE_KV)) break;
       if (lane == 0) {
-        mbar_expect_tx(bar(C::B_QFULL + s), 2 * TILE);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_3d(tb + C::T_Q + s * 2 * TILE + c * 128 * 128, &tmQ, bar(C::B_QFULL + s), c * 64, q0, bh);
-          tma_load_3d(tb + C::T_DO + s * 2 * TILE + c * 128 * 128, &tmdO, bar(C::B_QFULL + s), c * 64, q0, bh);
+        mbar_expect_tx(bar(C::B_QFULL + s), 2 * C::TD);
+        for (int c = 0; c < C::NCH; ++c) {
+          tma_load_3d(tb + C::T_Q + s * 2 * C::TD + c * 128 * 128, &tmQ, bar(C::B_QFULL + s), c * 64, q0, bh);
+          tma_load_3d(tb + C::T_DO + s * 2 * C::TD + c * 128 * 128, &tmdO, bar(C::B_QFULL + s), c * 64, q0, bh);
         }
       }
       float* Ls = reinterpret_cast<float*>(smem_raw + C::OFF_LD + s * C::LD_BYTES);
@@ -145,21 +146,21 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
     bool ok = mbar_wait(bar(C::B_KV), 0, guard, SITE_KV);
     for (int it = 0; ok && it < n_it; ++it) {
       const int s = it & 1;
-      const uint32_t qb = tb + C::T_Q + s * 2 * TILE, db = tb + C::T_DO + s * 2 * TILE;
+      const uint32_t qb = tb + C::T_Q + s * 2 * C::TD, db = tb + C::T_DO + s * 2 * C::TD;
       const uint32_t rs = tmem + C::TM_R + 128 * s, rd = tmem + C::TM_R + 128 * (s ^ 1);
       if (!(ok = mbar_wait(bar(C::B_QFULL + s), (it >> 1) & 1, guard, SITE_KV))) break;
       // region s held dP^T of the last step: every element-wise thread has read it
       if (it > 0 && !(ok = mbar_wait(bar(C::B_DPCONS), (it - 1) & 1, guard, SITE_KV))) break;
       tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
+      for (int ks = 0; ks < D / 16; ++ks)
         mma_ss(rs, sdesc_kmajor<128, 128>(kb, ks), sdesc_kmajor<128, 128>(qb, ks), idKK, ks > 0);
       mma_commit(bar(C::B_SFULL));
       // region s^1 held P^T and dS^T of the last step until dV and dK read them
       if (it > 0 && !(ok = mbar_wait(bar(C::B_DKDONE), (it - 1) & 1, guard, SITE_KV))) break;
       tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
+      for (int ks = 0; ks < D / 16; ++ks)
         mma_ss(rd, sdesc_kmajor<128, 128>(vb, ks), sdesc_kmajor<128, 128>(db, ks), idKK, ks > 0);
       mma_commit(bar(C::B_DPFULL));
     }
@@ -167,11 +168,11 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
     if (ok && tile_counter != nullptr) atomicAdd(tile_counter, static_cast<unsigned long long>(n_it));
   } else if (warp == 2 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- issuer B: dV, dK
-    constexpr uint32_t idTN = idesc_bf16(128, 128, false, true);
+    constexpr uint32_t idTN = idesc_bf16(128, D, false, true);
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
       const int s = it & 1;
-      const uint32_t qb = tb + C::T_Q + s * 2 * TILE, db = tb + C::T_DO + s * 2 * TILE;
+      const uint32_t qb = tb + C::T_Q + s * 2 * C::TD, db = tb + C::T_DO + s * 2 * C::TD;
       const uint32_t rs = tmem + C::TM_R + 128 * s;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -295,9 +296,11 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const float f = t == 0 ? scale : 1.f;
-        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (krow0 + key) * 128 + 32 * qq;
+        // this warp's D / 4 columns of d
+        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (krow0 + key) * D + (D / 4) * qq;
         uint32_t r[32];
-        tmem_ld32(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 32 * qq, r);
+        if constexpr (D == 128) tmem_ld32(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 32 * qq, r);
+        else tmem_ld16(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 16 * qq, r);
         tmem_ld_wait<32>(r);
         if (n_it == 0) {  // no query sees these keys: the accumulators were never written
 #pragma unroll
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
         if (key < Nk) {
           uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < D / 32; ++i)
             d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * f, __uint_as_float(r[8 * i + 1]) * f),
                                pack_bf16x2(__uint_as_float(r[8 * i + 2]) * f, __uint_as_float(r[8 * i + 3]) * f),
                                pack_bf16x2(__uint_as_float(r[8 * i + 4]) * f, __uint_as_float(r[8 * i + 5]) * f),
@@ -331,7 +334,9 @@ __global__ void __launch_bounds__(KVC::NTHREADS, 1)
 }
 
 // ============================================================================ dQ
+template <int D>
 struct QC {
+  static constexpr int TD = 128 * D * 2, NCH = D / 64;
   static constexpr int NTHREADS = 640, NCOMP = 512;  // 4 + 16 element-wise warps
   // K_j lives until dQ_j is done, V_j only until dP_j is: three K stages and two
   // V stages let each load start two steps ahead of its use.
@@ -343,19 +348,19 @@ struct QC {
   };
   static constexpr int OFF_MISC = NBAR * 8;
   static constexpr int SMALL = 256;
-  static constexpr int T_Q = 0, T_DO = TILE, T_K = 2 * TILE, T_V = (2 + KST) * TILE;  // stage k: + k TILE
-  static constexpr int TILES = (2 + KST + VST) * TILE;
+  static constexpr int T_Q = 0, T_DO = TD, T_K = 2 * TD, T_V = (2 + KST) * TD;  // stage k: + k TD
+  static constexpr int TILES = (2 + KST + VST) * TD;
   static constexpr int SMEM = SMALL + 1024 + TILES;
   static constexpr int TM_S = 0, TM_DP = 256, TM_DQ = 384;  // S buffer b at TM_S + 128 b
 };
 
-template <bool CAUSAL>
-__global__ void __launch_bounds__(QC::NTHREADS, 1)
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(QC<D>::NTHREADS, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                  const float* __restrict__ Lg, const float* __restrict__ Dg, __nv_bfloat16* __restrict__ dQ, int Nq, int Nk, int window,
                  float c_log2, float scale, int* status) {
-  using C = QC;
+  using C = QC<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw + C::SMALL);
   const uint32_t sb = smem_u32(smem_raw), tb = smem_u32(tiles);
@@ -405,8 +410,8 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
 
   if (warp == 0 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- producer
-    mbar_expect_tx(bar(C::B_QDO), 2 * TILE);
-    for (int c = 0; c < 2; ++c) {
+    mbar_expect_tx(bar(C::B_QDO), 2 * C::TD);
+    for (int c = 0; c < C::NCH; ++c) {
       tma_load_3d(tb + C::T_Q + c * 128 * 128, &tmQ, bar(C::B_QDO), c * 64, qt * 128, bh);
       tma_load_3d(tb + C::T_DO + c * 128 * 128, &tmdO, bar(C::B_QDO), c * 64, qt * 128, bh);
     }
@@ -414,14 +419,14 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
     for (int j = 0; j < n_kv; ++j) {
       const int k = j % C::KST, v = j & 1;
       if (!mbar_wait(bar(C::B_KEMPTY + k), ((j / C::KST) & 1) ^ 1, guard, SITE_Q)) break;
-      mbar_expect_tx(bar(C::B_KFULL + k), TILE);
-      for (int c = 0; c < 2; ++c)
-        tma_load_3d(tb + C::T_K + k * TILE + c * 128 * 128, &tmK, bar(C::B_KFULL + k), c * 64, (jlo + j) * 128, bh);
+      mbar_expect_tx(bar(C::B_KFULL + k), C::TD);
+      for (int c = 0; c < C::NCH; ++c)
+        tma_load_3d(tb + C::T_K + k * C::TD + c * 128 * 128, &tmK, bar(C::B_KFULL + k), c * 64, (jlo + j) * 128, bh);
       lastk = j;
       if (!mbar_wait(bar(C::B_VEMPTY + v), ((j >> 1) & 1) ^ 1, guard, SITE_Q)) break;
-      mbar_expect_tx(bar(C::B_VFULL + v), TILE);
-      for (int c = 0; c < 2; ++c)
-        tma_load_3d(tb + C::T_V + v * TILE + c * 128 * 128, &tmV, bar(C::B_VFULL + v), c * 64, (jlo + j) * 128, bh);
+      mbar_expect_tx(bar(C::B_VFULL + v), C::TD);
+      for (int c = 0; c < C::NCH; ++c)
+        tma_load_3d(tb + C::T_V + v * C::TD + c * 128 * 128, &tmV, bar(C::B_VFULL + v), c * 64, (jlo + j) * 128, bh);
       lastv = j;
     }
     if (*abort_flag) {
@@ -437,13 +442,13 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
     bool ok = mbar_wait(bar(C::B_QDO), 0, guard, SITE_Q);
     for (int j = 0; ok && j < n_kv; ++j) {
       const int s = j & 1, k = j % C::KST;
-      const uint32_t kb = tb + C::T_K + k * TILE, vb = tb + C::T_V + s * TILE;
+      const uint32_t kb = tb + C::T_K + k * C::TD, vb = tb + C::T_V + s * C::TD;
       if (!(ok = mbar_wait(bar(C::B_KFULL + k), (j / C::KST) & 1, guard, SITE_Q))) break;
       // S buffer s last held dS_{j-2}: dQ_{j-2} must have read it
       if (j >= 2 && !(ok = mbar_wait(bar(C::B_SFREE + s), ((j >> 1) & 1) ^ 1, guard, SITE_Q))) break;
       tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
+      for (int ks = 0; ks < D / 16; ++ks)
         mma_ss(tmem + C::TM_S + 128 * s, sdesc_kmajor<128, 128>(qb, ks), sdesc_kmajor<128, 128>(kb, ks), idKK, ks > 0);
       mma_commit(bar(C::B_SFULL + s));
       // the dP columns are free once every element-wise thread has read dP_{j-1}
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
       if (!(ok = mbar_wait(bar(C::B_VFULL + s), (j >> 1) & 1, guard, SITE_Q))) break;
       tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
+      for (int ks = 0; ks < D / 16; ++ks)
         mma_ss(tmem + C::TM_DP, sdesc_kmajor<128, 128>(db, ks), sdesc_kmajor<128, 128>(vb, ks), idKK, ks > 0);
       mma_commit(bar(C::B_DPFULL));
       mma_commit(bar(C::B_VEMPTY + s));
@@ -459,11 +464,11 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
     mma_commit(bar(C::B_ADONE));
   } else if (warp == 2 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- issuer B: dQ
-    constexpr uint32_t idTN = idesc_bf16(128, 128, false, true);  // dS (tensor memory) x K (N-major)
+    constexpr uint32_t idTN = idesc_bf16(128, D, false, true);  // dS (tensor memory) x K (N-major)
     bool ok = true;
     for (int j = 0; ok && j < n_kv; ++j) {
       const int s = j & 1, k = j % C::KST;
-      const uint32_t kb = tb + C::T_K + k * TILE;
+      const uint32_t kb = tb + C::T_K + k * C::TD;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         if (!(ok = mbar_wait(bar(C::B_DSREADY + 2 * s + c), (j >> 1) & 1, guard, SITE_Q))) break;
@@ -549,12 +554,13 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
     if (ok) {
       tc_fence_after();
       uint32_t r[32];
-      tmem_ld32(tl + C::TM_DQ + 32 * kq, r);
+      if constexpr (D == 128) tmem_ld32(tl + C::TM_DQ + 32 * kq, r);
+      else tmem_ld16(tl + C::TM_DQ + 16 * kq, r);
       tmem_ld_wait<32>(r);
       if (q < Nq) {
-        uint4* d4 = reinterpret_cast<uint4*>(dQ + (row0 + q) * 128 + 32 * kq);
+        uint4* d4 = reinterpret_cast<uint4*>(dQ + (row0 + q) * D + (D / 4) * kq);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < D / 32; ++i)
           d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * scale, __uint_as_float(r[8 * i + 1]) * scale),
                              pack_bf16x2(__uint_as_float(r[8 * i + 2]) * scale, __uint_as_float(r[8 * i + 3]) * scale),
                              pack_bf16x2(__uint_as_float(r[8 * i + 4]) * scale, __uint_as_float(r[8 * i + 5]) * scale),
@@ -577,25 +583,25 @@ __global__ void __launch_bounds__(QC::NTHREADS, 1)
   }
 }
 
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 fa_status launch_t(const BwdLaunch& a, void* dQ) {
   CUtensorMap mQ, mK, mV, mdO;
-  if (!encode_bf16_3d(&mQ, a.Q, 128, a.Nq, a.BH, 64, 128) || !encode_bf16_3d(&mdO, a.dO, 128, a.Nq, a.BH, 64, 128) ||
-      !encode_bf16_3d(&mK, a.K, 128, a.Nk, a.BH, 64, 128) || !encode_bf16_3d(&mV, a.V, 128, a.Nk, a.BH, 64, 128))
+  if (!encode_bf16_3d(&mQ, a.Q, D, a.Nq, a.BH, 64, 128) || !encode_bf16_3d(&mdO, a.dO, D, a.Nq, a.BH, 64, 128) ||
+      !encode_bf16_3d(&mK, a.K, D, a.Nk, a.BH, 64, 128) || !encode_bf16_3d(&mV, a.V, D, a.Nk, a.BH, 64, 128))
     return FA_ERR_CUDA;
-  static_assert(KVC::SMEM <= SMEM_MAX && QC::SMEM <= SMEM_MAX, "shared memory budget");
-  auto kkv = bwd_kv_kernel<CAUSAL>;
-  auto kq = bwd_q_kernel<CAUSAL>;
-  if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, KVC::SMEM) != cudaSuccess ||
-      cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, QC::SMEM) != cudaSuccess)
+  static_assert(KVC<D>::SMEM <= SMEM_MAX && QC<D>::SMEM <= SMEM_MAX, "shared memory budget");
+  auto kkv = bwd_kv_kernel<D, CAUSAL>;
+  auto kq = bwd_q_kernel<D, CAUSAL>;
+  if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, KVC<D>::SMEM) != cudaSuccess ||
+      cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, QC<D>::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
   const int Tq = (a.Nq + 127) / 128, Tk = (a.Nk + 127) / 128;
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  kkv<<<dim3(Tk, a.BH), KVC::NTHREADS, KVC::SMEM, a.stream>>>(
+  kkv<<<dim3(Tk, a.BH), KVC<D>::NTHREADS, KVC<D>::SMEM, a.stream>>>(
       mQ, mK, mV, mdO, a.L, a.D, static_cast<__nv_bfloat16*>(a.dK), static_cast<__nv_bfloat16*>(a.dV), a.Nq, a.Nk,
       a.window, c_log2, a.scale, a.status, a.counter);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  kq<<<dim3(Tq, a.BH), QC::NTHREADS, QC::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D,
+  kq<<<dim3(Tq, a.BH), QC<D>::NTHREADS, QC<D>::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D,
                                                            static_cast<__nv_bfloat16*>(dQ), a.Nq, a.Nk, a.window,
                                                            c_log2, a.scale, a.status);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -603,8 +609,12 @@ fa_status launch_t(const BwdLaunch& a, void* dQ) {
 
 }  // namespace
 
-fa_status launch_bwd_two_kernel_d128(const BwdLaunch& a, void* dQ) {
-  return a.causal ? launch_t<true>(a, dQ) : launch_t<false>(a, dQ);
+fa_status launch_bwd_two_kernel(const BwdLaunch& a, void* dQ) {
+  switch (a.d) {
+    case 64: return a.causal ? launch_t<64, true>(a, dQ) : launch_t<64, false>(a, dQ);
+    case 128: return a.causal ? launch_t<128, true>(a, dQ) : launch_t<128, false>(a, dQ);
+    default: return FA_ERR_UNSUPPORTED;
+  }
 }
 
 }  // namespace fa

@@ -92,9 +92,9 @@ struct BwdLaunch {
 };
 fa_status launch_bwd(const BwdLaunch& a);
 fa_status launch_bwd_d128(const BwdLaunch& a);
-// Two-kernel backward (d = 128): dK, dV by key tile, then dQ by query tile,
+// Two-kernel backward (d = 64 or 128): dK, dV by key tile, then dQ by query tile,
 // written directly to dQ (bf16); needs no workspace.
-fa_status launch_bwd_two_kernel_d128(const BwdLaunch& a, void* dQ);
+fa_status launch_bwd_two_kernel(const BwdLaunch& a, void* dQ);
 
 fa_status launch_preprocess(const void* O, const void* dO, float* D, long long rows, int d, cudaStream_t s);
 fa_status launch_dq_convert(const float* dQacc, void* dQ, long long n, float scale, cudaStream_t s);

@@ -157,8 +157,12 @@ fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, 
  * Same arguments, results and errors as fa_bwd, without the workspace: the fp32
  * dQ accumulator is a fixed array inside the library (one per device that
  * loads it, held until the process exits), so the call allocates nothing.
- *   - Returns FA_ERR_WORKSPACE, without enqueuing anything, when
- *     B*H*N*d*4 > FA_NOALLOC_MAX_WORKSPACE_BYTES.
+ *   - Returns FA_ERR_WORKSPACE, without enqueuing anything, when the backward
+ *     that runs needs an accumulator larger than the array:
+ *     fa_bwd_workspace_size() > FA_NOALLOC_MAX_WORKSPACE_BYTES, i.e.
+ *     B*H*N*d*4 bytes for the one-kernel form (d = 32, d = 128 by default).
+ *     The two-kernel form (d = 64 by default) uses no accumulator and no
+ *     array, and has no such limit.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.
@@ -205,15 +209,15 @@ long long fa_tile_pairs_ex(int Nq, int Nk, int d, int causal, int window, int pa
 fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter);
 
 /*
- * Debug: which form of the backward fa_bwd runs for d = 128 ("CS336
+ * Debug: which form of the backward fa_bwd runs for d = 64 and 128 ("CS336
  * Assignment 2 notes" §1.4 leaves the split open):
  *   1: one kernel, key/value tiles outer; dQ accumulated in the fp32 workspace
  *      and rounded to bf16 by a second pass;
  *   2: two kernels, key/value tiles outer for dK and dV, then query tiles outer
  *      for dQ (S and P recomputed in both); no workspace, no reductions;
- *   0: the library's default (the faster of the two on GB300).
- * d = 32 and 64 always run form 1.  Process-wide setting; FA_ERR_INVALID_ARG
- * for other values.
+ *   0: the library's default (the faster of the two on GB300 for each d).
+ * d = 32 always runs form 1.  Process-wide setting; FA_ERR_INVALID_ARG for
+ * other values.
  */
 fa_status fa_debug_set_bwd_split(int split);
 

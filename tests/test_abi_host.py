@@ -64,8 +64,9 @@ def test_argument_errors_before_any_cuda_call(fa_lib):
     assert fa.fa_fwd(p, p, p, p, p, -1, 1, 64, 64, 0, 0.1, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_fwd(p, p, p, p, p, 1024, 1024, 64, 64, 0, 0.1, None) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_bwd_preprocess(None, p, p, 1, 1, 8, 32, None) == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_bwd(p, p, p, p, p, p, p, p, p, p, 1, 1, 64, 64, 1, 0.1, None, 0, None) == fa.FA_ERR_WORKSPACE
-    assert fa.fa_bwd(p, p, p, p, p, p, p, p, p, p, 1, 1, 64, 64, 1, 0.1, p, 100, None) == fa.FA_ERR_WORKSPACE
+    # d = 32 runs the one-kernel backward, which needs the fp32 dQ workspace
+    assert fa.fa_bwd(p, p, p, p, p, p, p, p, p, p, 1, 1, 64, 32, 1, 0.1, None, 0, None) == fa.FA_ERR_WORKSPACE
+    assert fa.fa_bwd(p, p, p, p, p, p, p, p, p, p, 1, 1, 64, 32, 1, 0.1, p, 100, None) == fa.FA_ERR_WORKSPACE
     assert fa.fa_debug_timeout_probe(0, None) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_selftest_umma(7, p, p, p, 64, 64, None) == fa.FA_ERR_INVALID_ARG
 
@@ -115,14 +116,15 @@ def test_tile_pair_counts_for_the_workloads(fa_lib):
 
 def test_backward_split_selection(fa_lib):
     """Form 2 (two kernels) writes dQ directly and needs no workspace; form 1 needs
-    the fp32 dQ accumulator; d = 32 and 64 always use form 1."""
+    the fp32 dQ accumulator; d = 32 always uses form 1."""
     fa = fa_lib
     try:
         assert fa.fa_debug_set_bwd_split(3) == fa.FA_ERR_INVALID_ARG
         assert fa.fa_debug_set_bwd_split(-1) == fa.FA_ERR_INVALID_ARG
         assert fa.fa_debug_set_bwd_split(2) == fa.FA_OK
         assert fa.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 0
-        assert fa.fa_bwd_workspace_size(2, 16, 4096, 64, 1) == 2 * 16 * 4096 * 64 * 4
+        assert fa.fa_bwd_workspace_size(2, 16, 4096, 64, 1) == 0
+        assert fa.fa_bwd_workspace_size(2, 16, 4096, 32, 1) == 2 * 16 * 4096 * 32 * 4
         assert fa.fa_debug_set_bwd_split(1) == fa.FA_OK
         assert fa.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 2 * 16 * 4096 * 128 * 4
     finally:
@@ -155,7 +157,8 @@ def test_masked_argument_errors(fa_lib):
     assert fa.fa_fwd_ex(None, None, None, None, None, 1, 1, 0, 64, 64, 1, 8, 0.1, None) == fa.FA_OK  # no queries
     assert fa.fa_tile_pairs_ex(65, 64, 128, 1, 0, 0) == -1
     assert fa.fa_tile_pairs_ex(64, 64, 128, 0, 8, 0) == -1
-    assert fa.fa_bwd_workspace_size_ex(2, 3, 100, 700, 64, 1, 50) == 2 * 3 * 100 * 64 * 4
+    assert fa.fa_bwd_workspace_size_ex(2, 3, 100, 700, 32, 1, 50) == 2 * 3 * 100 * 32 * 4
+    assert fa.fa_bwd_workspace_size_ex(2, 3, 100, 700, 64, 1, 50) == 0  # d = 64: two kernels, no workspace
     assert fa.fa_bwd_workspace_size_ex(2, 3, 100, 700, 64, 0, 50) == ctypes.c_size_t(-1).value
     for N, c in ((1000, 0), (1000, 1), (129, 1)):
         for pass_ in (0, 1):

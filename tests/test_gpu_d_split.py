@@ -1,4 +1,4 @@
-"""GPU parity of both forms of the d = 128 backward ("CS336 Assignment 2 notes"
+"""GPU parity of both forms of the d = 64 and d = 128 backward ("CS336 Assignment 2 notes"
 §1.4): form 1 (one kernel over key tiles, dQ reduced in an fp32 workspace) and
 form 2 (a key-tile kernel for dK, dV and a query-tile kernel for dQ), each
 against the float64 oracle, whichever of them is the library's default."""
@@ -25,23 +25,25 @@ def _grads(got):
     return {n: f64(got[n]) for n in ("dQ", "dK", "dV")}
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("split", SPLITS)
 @pytest.mark.parametrize("N", [1, 7, 100, 128, 129, 300, 1000])
 @pytest.mark.parametrize("causal", [False, True])
-def test_ragged_lengths(split, N, causal):
-    Q, K, V, dO = si.make_qkvdo(1, 2, N, 128, seed=300 + N)
+def test_ragged_lengths(d, split, N, causal):
+    Q, K, V, dO = si.make_qkvdo(1, 2, N, d, seed=300 + N + d)
     got = run_gpu(Q, K, V, dO, causal, counter=True, split=split)
     ref = _oracle_full(Q, K, V, dO, causal)
-    assert_close(_grads(got), {n: ref[n] for n in ("dQ", "dK", "dV")}, f"split={split} N={N} causal={causal}")
+    assert_close(_grads(got), {n: ref[n] for n in ("dQ", "dK", "dV")}, f"d={d} split={split} N={N} causal={causal}")
     # the key-tile kernel counts the pairs it computed: the closed form's
-    assert got["tiles"][1] == 2 * lib().fa_tile_pairs(N, 128, causal, 1)
+    assert got["tiles"][1] == 2 * lib().fa_tile_pairs(N, d, causal, 1)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("split", SPLITS)
 @pytest.mark.parametrize("causal", [False, True])
-def test_large_logits_and_scale(split, causal):
+def test_large_logits_and_scale(d, split, causal):
     """Scores ~16x unit variance and a scale other than 1/sqrt(d)."""
-    Q, K, V, dO = si.make_qkvdo(2, 2, 640, 128, seed=31, qk_mult=4.0)
+    Q, K, V, dO = si.make_qkvdo(2, 2, 640, d, seed=31, qk_mult=4.0)
     got = run_gpu(Q, K, V, dO, causal, scale=0.05, split=split)
     ref = _oracle_full(Q, K, V, dO, causal, scale=0.05)
     assert_close(_grads(got), {n: ref[n] for n in ("dQ", "dK", "dV")}, f"split={split} qk x4")
@@ -76,3 +78,14 @@ def test_forms_agree_and_form2_is_deterministic(causal):
     for n in ("dQ", "dK", "dV"):
         assert rel_frob(f64(b[n]), f64(a[n])) <= 1e-2, n
         assert (b[n] == c[n]).all(), n
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_small_workload_form2_d64(causal):
+    """The small workload (4 x 8 heads x 1024 x 64) through form 2, every gradient."""
+    w = si.WORKLOADS["small_4x8x1024x64"]
+    Q, K, V, dO = si.make_workload(w)
+    got = run_gpu(Q, K, V, dO, causal, counter=True, split=2)
+    ref = _oracle_full(Q, K, V, dO, causal)
+    assert_close(_grads(got), {n: ref[n] for n in ("dQ", "dK", "dV")}, "small form 2")
+    assert got["tiles"][1] == 32 * lib().fa_tile_pairs(1024, 64, causal, 1)

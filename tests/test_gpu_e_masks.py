@@ -49,10 +49,11 @@ def test_sliding_window(d, N, window):
     _check(N, N, d, True, window, seed=400 + N + window + d)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("split", [1, 2])
 @pytest.mark.parametrize("N,window", [(1000, 100), (777, 256), (300, 1)])
-def test_sliding_window_both_backward_forms(split, N, window):
-    _check(N, N, 128, True, window, seed=500 + N + window, split=split)
+def test_sliding_window_both_backward_forms(d, split, N, window):
+    _check(N, N, d, True, window, seed=500 + N + window, split=split)
 
 
 @pytest.mark.parametrize("d", [64, 128])
@@ -64,10 +65,12 @@ def test_unequal_lengths(d, Nq, Nk, causal, window):
     _check(Nq, Nk, d, causal, window, seed=600 + Nq + Nk + d)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("split", [1, 2])
-def test_unequal_lengths_both_backward_forms(split):
-    _check(300, 1000, 128, True, 0, seed=700, split=split)
-    _check(1000, 300, 128, False, 0, seed=701, split=split)
+def test_unequal_lengths_both_backward_forms(d, split):
+    _check(300, 1000, d, True, 0, seed=700, split=split)
+    _check(1000, 300, d, False, 0, seed=701, split=split)
+    _check(64, 1000, d, True, 32, seed=702, split=split)
 
 
 @pytest.mark.parametrize("d", [64, 128])
