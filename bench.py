@@ -238,14 +238,35 @@ def cpu_oracle_sample(w: si.Workload, causal: bool, budget_s: float = 12.0, max_
                       f"{dt:.2f} s for {f / 1e9:.1f} GFLOP counted"}
 
 
+def rank_env():
+    """(world size, rank, local rank) from the launcher's environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(ms, dist, device):
+    """The slowest rank's timed region: every rank gets the maximum (no-op alone)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step, steps, world, total_ms):
+    """Throughput of the whole job: every rank runs a full replica of the step
+    (weak scaling, no data-path collective), so the job does world times the work
+    in the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (total_ms / 1e3) / 1e12
+
+
 def run_ours(args):
     import torch
 
     import exact_tiled_attention_26_gb300 as fa
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -272,13 +293,9 @@ def run_ours(args):
         fwd_ms, bwd_ms = time_steps(torch, r, args.steps, 0)
     st, detail = fa.fa_poll_device_error(r.s)
     fa.check(st, f"device status word (site {detail:#x})")
-    total_ms = fwd_ms + bwd_ms
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(fwd_ms + bwd_ms, dist, dev)
     ms_step = total_ms / args.steps
-    value = world * (flops_f + flops_b) * args.steps / (total_ms / 1e3) / 1e12
+    value = whole_job_tflops(flops_f + flops_b, args.steps, world, total_ms)
 
     peaks, peak_src = _peaks()
     sustained = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
@@ -378,15 +395,15 @@ def per_config(fa, torch, dev, peaks):
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    _, rank, _ = rank_env()
+    if rank != 0:  # under torchrun only rank 0 times the oracle
         return
     w = si.WORKLOADS[args.workload]
     causal = True
     import oracle
     Q, K, V, dO = si.make_qkvdo(1, 1, w.N, w.d, seed=w.seed, qk_mult=w.qk_mult)
     q, k, v, do = (si.to_f64(t)[0, 0] for t in (Q, K, V, dO))
-    n = 2048  # rows 0..n-1 of head 0: an exact causal sub-problem of the workload
+    n = min(2048, w.N)  # rows 0..n-1 of head 0: an exact causal sub-problem of the workload
     flops = 14.0 * n * n * w.d * 0.5
 
     def step():
