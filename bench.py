@@ -41,7 +41,7 @@ UNIT = "TFLOP/s"
 # backward main kernel, from the ncu capture summarised in
 # profiles/launches_vlong_1x32x32768x128_causal.md; valid for the kernel as captured
 # there (set to None whenever the kernel changes).
-_TRAFFIC = {("vlong_1x32x32768x128", True): 1621248000 + 1023066368}
+_TRAFFIC = {}
 
 
 def _peaks():

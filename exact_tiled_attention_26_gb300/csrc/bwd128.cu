@@ -59,7 +59,8 @@ struct B128 {
     B_KV = 0, B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6,
     B_PREADY = 7,  // [step parity][sub-chunk]: the element-wise warps may be a step ahead of issuer B
     B_DSREADY = 11, B_DKDONE = 13, B_DQFULL = 14, B_DQCONS = 15, B_DPCONS = 16, B_FINAL = 17, B_ADONE = 18,
-    NBAR = 19
+    B_DSSMEM = 19,  // dS^T of the step is in shared memory (for dQ^T)
+    NBAR = 20
   };
   static constexpr int OFF_BAR = 0;
   static constexpr int OFF_MISC = NBAR * 8;     // tensor-memory base, abort flag
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       mbar_init(bar(C::B_DSREADY + c), C::NCOMP);
     }
     mbar_init(bar(C::B_DPCONS), C::NCOMP);
+    mbar_init(bar(C::B_DSSMEM), C::NCOMP);
     mbar_init(bar(C::B_DKDONE), 1);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQCONS), C::NDQ);
@@ -269,6 +271,7 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
       // dQ_i^T = K^T dS^T (both from shared memory) over region s, once dV and dK have
       // read its P^T and dS^T
       if (!(ok = mbar_wait(bar(C::B_DKDONE), it & 1, guard, SITE_MMA))) break;
+      if (!(ok = mbar_wait(bar(C::B_DSSMEM), it & 1, guard, SITE_MMA))) break;
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
@@ -412,10 +415,12 @@ __global__ void __launch_bounds__(B128::NTHREADS, 1)
           *reinterpret_cast<uint4*>(row + (((4 * c + u) ^ (kr & 7)) << 4)) =
               make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
         tmem_st_wait();
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(bar(C::B_DSREADY + c));
+        mbar_arrive(bar(C::B_DSREADY + c));  // dK reads dS^T from tensor memory
       }
+      // dQ^T reads dS^T from shared memory: one proxy fence for both sub-chunks
+      fence_proxy_async_smem();
+      mbar_arrive(bar(C::B_DSSMEM));
 
     }
     // dK (times scale) and dV: this warp's lane quarter, d columns 64h .. 64h+63
