@@ -20,9 +20,10 @@ __all__ = [
     "FAError", "lib", "lib_path", "fa_fwd", "fa_bwd_preprocess", "fa_bwd_workspace_size", "fa_bwd",
     "fa_fwd_ex", "fa_bwd_ex", "fa_bwd_workspace_size_ex", "fa_tile_pairs_ex",
     "fa_bwd_noalloc", "FA_NOALLOC_MAX_WORKSPACE_BYTES",
+    "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host_chunk_heads",
     "fa_status_string", "fa_get_tile_config", "fa_tile_pairs", "fa_debug_set_tile_counter", "fa_debug_set_bwd_split",
     "fa_poll_device_error", "fa_debug_timeout_probe", "fa_selftest_umma", "fa_version",
-    "attention_forward", "attention_backward", "check",
+    "attention_forward", "attention_backward", "attention_fwd_bwd_host", "check",
 ]
 
 FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT, FA_ERR_WORKSPACE = range(6)
@@ -58,6 +59,9 @@ _sig = {
     "fa_bwd_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "fa_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "fa_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]),
+    "fa_fwd_bwd_host_chunk_heads": (_i, [_i] * 6),
+    "fa_fwd_bwd_host_workspace_size": (_sz, [_i] * 8),
+    "fa_fwd_bwd_host": (_i, [_vp] * 9 + [_i] * 7 + [_f, _i, _vp, _sz, _vp]),
     "fa_status_string": (ctypes.c_char_p, [_i]),
     "fa_get_tile_config": (_i, [_i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]),
     "fa_tile_pairs": (ctypes.c_longlong, [_i, _i, _i, _i]),
@@ -117,6 +121,21 @@ def fa_bwd_noalloc(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, N, d, causal, scale, 
     """fa_bwd without a caller-provided workspace (see include/fa.h): for callers
     that cannot allocate device memory; limited to B*H*N*d*4 <= 16 MiB."""
     return lib.fa_bwd_noalloc(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, N, d, int(bool(causal)), scale, stream)
+
+
+def fa_fwd_bwd_host_chunk_heads(B, H, Nq, Nk, d, heads_per_chunk):
+    return lib.fa_fwd_bwd_host_chunk_heads(B, H, Nq, Nk, d, heads_per_chunk)
+
+
+def fa_fwd_bwd_host_workspace_size(B, H, Nq, Nk, d, causal, window, heads_per_chunk):
+    return lib.fa_fwd_bwd_host_workspace_size(B, H, Nq, Nk, d, int(bool(causal)), window, heads_per_chunk)
+
+
+def fa_fwd_bwd_host(Q, K, V, dO, O, L, dQ, dK, dV, B, H, Nq, Nk, d, causal, window, scale, heads_per_chunk, workspace,
+                    workspace_bytes, stream):
+    """Forward + backward on host arrays, copies overlapped with the kernels (see include/fa.h)."""
+    return lib.fa_fwd_bwd_host(Q, K, V, dO, O, L, dQ, dK, dV, B, H, Nq, Nk, d, int(bool(causal)), window, scale,
+                               heads_per_chunk, workspace, workspace_bytes, stream)
 
 
 def fa_status_string(status):
@@ -220,3 +239,36 @@ def attention_backward(q, k, v, o, lse, do, causal=False, scale=None, window=0, 
                     D.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, causal, window, scale,
                     workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream), "fa_bwd_ex")
     return dq, dk, dv, D
+
+
+def attention_fwd_bwd_host(q, k, v, do, causal=False, scale=None, window=0, heads_per_chunk=0, device=None):
+    """O, L, dQ, dK, dV of exact attention for bf16 CPU tensors q, do [B,H,Nq,d] and
+    k, v [B,H,Nk,d], computed on `device` (default: the current CUDA device) by
+    fa_fwd_bwd_host.  Returns page-locked CPU tensors once the step has finished.
+    Page-locked inputs (Tensor.pin_memory()) let the copies overlap the kernels."""
+    import torch
+    for t in (q, k, v, do):
+        if t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError("expected contiguous bf16 CPU tensors of shape [B, H, N, d]")
+    if k.shape != v.shape or k.shape[:2] != q.shape[:2] or k.shape[3] != q.shape[3] or do.shape != q.shape:
+        raise ValueError("K and V must be [B, H, Nk, d] with the B, H and d of Q; dO must have the shape of Q")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws_bytes = fa_fwd_bwd_host_workspace_size(B, H, Nq, Nk, d, causal, window, heads_per_chunk)
+    if ws_bytes == ctypes.c_size_t(-1).value:
+        check(FA_ERR_INVALID_ARG, "fa_fwd_bwd_host_workspace_size")
+    with torch.cuda.device(device):
+        ws = torch.empty(max(ws_bytes + 256, 256), dtype=torch.uint8, device=device)
+        base = (ws.data_ptr() + 255) // 256 * 256
+        o, dq = (torch.empty(q.shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2))
+        dk, dv = (torch.empty(k.shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2))
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, pin_memory=True)
+        stream = torch.cuda.current_stream(device)
+        check(fa_fwd_bwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), do.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, causal, window, scale,
+                              heads_per_chunk, base, ws_bytes, stream.cuda_stream), "fa_fwd_bwd_host")
+        stream.synchronize()
+        del ws
+    return o, lse, dq, dk, dv

@@ -65,6 +65,14 @@ fa_status check_shape(int B, int H, int N, int d, bool* empty) {
   return FA_OK;
 }
 
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+}  // namespace
+
 // Shape and mask checks of the general-mask entry points.  *empty: no query rows
 // (or no heads), so no attention is computed.
 fa_status check_mask_shape(int B, int H, int Nq, int Nk, int d, int causal, int window, bool* empty) {
@@ -82,14 +90,6 @@ fa_status check_mask_shape(int B, int H, int Nq, int Nk, int d, int causal, int 
 }
 
 bool check_scale(float scale) { return std::isfinite(scale) && scale > 0.f; }
-
-int current_device() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-  return dev;
-}
-
-}  // namespace
 
 int* device_status_word() {
   const int dev = current_device();

@@ -54,6 +54,12 @@ __host__ __device__ inline void query_tile_range(int kt, int Br, int Bc, int Nq,
   *hi = h;
 }
 
+// Shape and mask checks of the general-mask entry points (fa_fwd_ex's rules);
+// *empty is set when there are no query rows or no heads.
+fa_status check_mask_shape(int B, int H, int Nq, int Nk, int d, int causal, int window, bool* empty);
+// scale finite and > 0.
+bool check_scale(float scale);
+
 // Device status word of the current device (see fa_poll_device_error).
 int* device_status_word();
 

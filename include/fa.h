@@ -174,6 +174,44 @@ fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void
                          const float* L, const float* D, void* dQ, void* dK, void* dV,
                          int B, int H, int N, int d, int causal, float scale, fa_stream_t stream);
 
+/*
+ * One forward + backward step of exact attention on HOST-resident tensors: O,
+ * L, dQ, dK, dV from Q, K, V, dO, exactly as fa_fwd_ex, fa_bwd_preprocess and
+ * fa_bwd_ex compute them (same mask rules, same kernels), with every host <->
+ * device copy inside the call.  The pages run both passes on device arrays; this
+ * entry point is for callers whose tensors live in host memory, and it hides the
+ * copies behind the kernels: the B*H heads go through in chunks, and while one
+ * chunk computes, the next chunk's inputs come in and the previous chunk's
+ * results go out, on streams internal to the library.
+ *
+ *   Q, dO: bf16 host [B,H,Nq,d]; K, V: bf16 host [B,H,Nk,d]; outputs O, dQ: bf16
+ *   host [B,H,Nq,d]; dK, dV: bf16 host [B,H,Nk,d]; L: fp32 host [B,H,Nq].  Host
+ *   arrays should be page-locked (cudaHostAlloc, cudaHostRegister) for the copies
+ *   to run asynchronously and overlap the kernels; pageable arrays give the same
+ *   results with the copies serialised.
+ *   heads_per_chunk: heads of the flattened B*H per chunk; 0 lets the library
+ *   choose (fa_fwd_bwd_host_chunk_heads tells which).
+ *   workspace: fa_fwd_bwd_host_workspace_size() bytes of device memory, 256-byte
+ *   aligned (FA_ERR_WORKSPACE otherwise): device copies of up to four chunks and
+ *   two dQ accumulators.  Calls that share a workspace must be ordered (the same
+ *   stream, or synchronised).
+ *   stream: the step is ordered after the work already on `stream`, and work
+ *   enqueued on `stream` later is ordered after the last copy back.  The call
+ *   returns once all of it is enqueued; the host outputs are valid, and the host
+ *   inputs may change again, after `stream` is synchronised.
+ * Argument errors return before anything is enqueued; a CUDA failure midway
+ * returns FA_ERR_CUDA with part of the step enqueued.
+ * fa_fwd_bwd_host_chunk_heads and fa_fwd_bwd_host_workspace_size are host only
+ * (no GPU needed) and return -1 (as size_t for the second) on bad arguments.
+ */
+int fa_fwd_bwd_host_chunk_heads(int B, int H, int Nq, int Nk, int d, int heads_per_chunk);
+size_t fa_fwd_bwd_host_workspace_size(int B, int H, int Nq, int Nk, int d, int causal, int window,
+                                      int heads_per_chunk);
+fa_status fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const void* dO,
+                          void* O, float* L, void* dQ, void* dK, void* dV,
+                          int B, int H, int Nq, int Nk, int d, int causal, int window, float scale,
+                          int heads_per_chunk, void* workspace, size_t workspace_bytes, fa_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(fa_status s);
 

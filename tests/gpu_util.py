@@ -12,10 +12,16 @@ bound on O therefore applies to the error beyond that quantum:
 |got - ref| - ulp_bf16(ref)/2 <= 1e-2.  A gradient whose exact value is zero
 (e.g. dQ and dK with a single key) is checked by its RMS (<= 1e-4) instead of
 the relative norm.
+
+With FA_PARITY_LOG set to a file name, every comparison appends its measured
+errors to that file as one JSON line (O: max-abs, max-abs beyond half a bf16
+ulp, rel-Frobenius; L: max-abs; gradients: rel-Frobenius).
 """
 from __future__ import annotations
 
+import json
 import math
+import os
 
 import numpy as np
 import torch
@@ -122,6 +128,10 @@ def assert_close(got: dict, ref: dict, label=""):
             errs[n] = er
             if not er <= TOL_G_REL:
                 msgs.append(f"{n} rel {er:.3e}")
+    log = os.environ.get("FA_PARITY_LOG")
+    if log:  # measured errors, one JSON line per comparison, for the record of a run
+        with open(log, "a") as f:
+            f.write(json.dumps({"case": label, "pass": not msgs, "errs": errs}) + "\n")
     assert not msgs, f"{label}: " + "; ".join(msgs)
     return errs
 
