@@ -50,7 +50,7 @@ def test_sampled_rows(name, causal):
     O, L, dQ, D = oracle.rows_fwd_bwd(q, k, v, do, rows, causal)
     g = {n: f64(_heads(got[n]) if got[n].dim() == 4 else got[n].reshape(-1, w.N))[:, rows]
          for n in ("O", "L", "dQ", "D")}
-    assert_close({"O": g["O"], "L": g["L"], "dQ": g["dQ"]}, {"O": O, "L": L, "dQ": dQ}, f"{name} rows")
+    assert_close({"O": g["O"], "L": g["L"], "dQ": g["dQ"]}, {"O": O, "L": L, "dQ": dQ}, f"{name} causal={causal} rows")
     assert rel_frob(g["D"], D) <= 1e-2
 
 
@@ -63,7 +63,7 @@ def test_whole_heads(name, causal):
         dQ, dK, dV, _ = oracle.standard_attention_bwd(q, k, v, do, causal)
         g = {n: f64(_heads(got[n])[h]) for n in ("O", "dQ", "dK", "dV")}
         g["L"] = f64(got["L"].reshape(-1, w.N)[h])
-        assert_close(g, {"O": O, "L": L, "dQ": dQ, "dK": dK, "dV": dV}, f"{name} head {h}")
+        assert_close(g, {"O": O, "L": L, "dQ": dQ, "dK": dK, "dV": dV}, f"{name} causal={causal} head {h}")
 
 
 def test_vlong_sampled_key_rows():
