@@ -22,6 +22,7 @@ __all__ = [
     "fa_bwd_noalloc", "FA_NOALLOC_MAX_WORKSPACE_BYTES",
     "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host_chunk_heads",
     "fa_status_string", "fa_get_tile_config", "fa_tile_pairs", "fa_debug_set_tile_counter", "fa_debug_set_bwd_split",
+    "fa_debug_set_fwd_form",
     "fa_poll_device_error", "fa_debug_timeout_probe", "fa_selftest_umma", "fa_version",
     "attention_forward", "attention_backward", "attention_fwd_bwd_host", "check",
 ]
@@ -67,6 +68,7 @@ _sig = {
     "fa_tile_pairs": (ctypes.c_longlong, [_i, _i, _i, _i]),
     "fa_debug_set_tile_counter": (_i, [_vp]),
     "fa_debug_set_bwd_split": (_i, [_i]),
+    "fa_debug_set_fwd_form": (_i, [_i]),
     "fa_poll_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
     "fa_debug_timeout_probe": (_i, [_i, _vp]),
     "fa_selftest_umma": (_i, [_i, _vp, _vp, _vp, _i, _i, _vp]),
@@ -158,6 +160,10 @@ def fa_debug_set_tile_counter(dev_counter):
 
 def fa_debug_set_bwd_split(split):
     return lib.fa_debug_set_bwd_split(split)
+
+
+def fa_debug_set_fwd_form(form):
+    return lib.fa_debug_set_fwd_form(form)
 
 
 def fa_poll_device_error(stream):

@@ -20,6 +20,7 @@ int* g_status_ptr[kMaxDevices] = {nullptr};
 std::mutex g_mu;
 unsigned long long* g_tile_counter = nullptr;
 int g_bwd_split = 0;                    // 0: the defaults below
+int g_fwd_form = 0;                     // 0: the default (fwd_form below)
 constexpr int kDefaultBwdSplitD128 = 1;  // chosen by measurement on GB300
 constexpr int kDefaultBwdSplitD64 = 2;  // two kernels: faster at d = 64 (measured)
 
@@ -188,6 +189,25 @@ fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter) {
   return FA_OK;
 }
 
+// Which forward kernel runs.  Measured on GB300: two query tiles per CTA (form 2)
+// is faster when every query tile sees at most 16 key tiles (short windows,
+// sequences up to 2048: +1% to +21%), the one-tile form with its deeper S buffering
+// when query tiles see more (up to 14% faster at 32 key tiles), and with fewer than
+// two query tiles per head form 2 has nothing to pair.
+static int fwd_form(int d, int Nq, int Nk, bool causal, int window) {
+  if (d != 128) return 1;
+  if (g_fwd_form != 0) return g_fwd_form;
+  const int T = (Nq + kFwdBr - 1) / kFwdBr;
+  if (T < 2) return 1;
+  for (int qt = T - 1; qt >= 0; --qt) {  // the widest ranges are at the end (causal) or inside (window)
+    int lo = 0, hi = -1;
+    key_tile_range(qt, kFwdBr, kFwdBc, Nq, Nk, causal, window, &lo, &hi);
+    if (hi - lo + 1 > 16) return 1;
+    if (window == 0) break;  // without a window the last query tile sees the most
+  }
+  return 2;
+}
+
 fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Nq, int Nk,
                     int d, int causal, int window, float scale, fa_stream_t stream) {
   bool empty = false;
@@ -201,7 +221,7 @@ fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float*
   int* status = device_status_word();
   if (status == nullptr) return FA_ERR_CUDA;
   FwdLaunch a{Q, K, V, O, L, B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
-  return launch_fwd(a);
+  return fwd_form(d, Nq, Nk, causal != 0, window) == 2 ? launch_fwd_pp(a) : launch_fwd(a);
 }
 
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
@@ -237,6 +257,12 @@ size_t fa_bwd_workspace_size_ex(int B, int H, int Nq, int Nk, int d, int causal,
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
   return fa_bwd_workspace_size_ex(B, H, N, N, d, causal, 0);
+}
+
+fa_status fa_debug_set_fwd_form(int form) {
+  if (form < 0 || form > 2) return FA_ERR_INVALID_ARG;
+  g_fwd_form = form;
+  return FA_OK;
 }
 
 fa_status fa_debug_set_bwd_split(int split) {

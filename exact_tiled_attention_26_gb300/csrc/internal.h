@@ -84,6 +84,8 @@ struct FwdLaunch {
   unsigned long long* counter;
 };
 fa_status launch_fwd(const FwdLaunch& a);
+// d = 128 forward with two query tiles per CTA (fwd_pp.cu).
+fa_status launch_fwd_pp(const FwdLaunch& a);
 
 struct BwdLaunch {
   const void *Q, *K, *V, *dO;

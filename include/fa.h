@@ -260,6 +260,17 @@ fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter);
 fa_status fa_debug_set_bwd_split(int split);
 
 /*
+ * Debug: which forward kernel fa_fwd runs for d = 128 (the same computation,
+ * "CS336 Assignment 2 notes" §1.2; other d always run form 1):
+ *   1: one 128-row query tile per CTA;
+ *   2: two query tiles per CTA whose softmax and tensor-core work take turns;
+ *   0: the library's default, chosen by measurement on GB300: form 2 when there
+ *      are at least two query tiles and none sees more than 16 key tiles, else 1.
+ * Process-wide setting; FA_ERR_INVALID_ARG for other values.
+ */
+fa_status fa_debug_set_fwd_form(int form);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  FA_OK if no kernel has given up since the last poll;
  * FA_ERR_TIMEOUT otherwise, with the failing wait site in *detail (may be NULL).

@@ -163,3 +163,11 @@ def test_masked_argument_errors(fa_lib):
     for N, c in ((1000, 0), (1000, 1), (129, 1)):
         for pass_ in (0, 1):
             assert fa.fa_tile_pairs_ex(N, N, 128, c, 0, pass_) == fa.fa_tile_pairs(N, 128, c, pass_)
+
+
+def test_forward_form_switch(fa_lib):
+    fa = fa_lib
+    for form in (0, 1, 2, 0):
+        assert fa.fa_debug_set_fwd_form(form) == fa.FA_OK
+    assert fa.fa_debug_set_fwd_form(3) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_set_fwd_form(-1) == fa.FA_ERR_INVALID_ARG
