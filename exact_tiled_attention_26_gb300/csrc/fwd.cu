@@ -17,21 +17,16 @@
 //               a hundred cycles even when the barrier is already complete, and
 //               the pipe's queue of UMMAs is too short to cover that.
 //   warps 4..7  softmax: one thread per query row (its tensor-memory lane);
-//               online max/sum in base 2 with the scale folded into one FMA,
-//               P written back as bf16 over its own S columns; epilogue
-// The accumulator is rescaled lazily: only when a row's max grows by more
-// than 8 (in base-2 units) is the running max moved and O, l multiplied by
-// 2^(m_old - m_new).  Between moves P <= 2^8, well inside fp32 and bf16 range;
-// O / l is unchanged by the choice of reference max.
+//               online max/sum in base 2 with the scale folded into one FMA and
+//               a lazily moved reference max, P written back as bf16 over its
+//               own S columns; epilogue (fwd_softmax.cuh)
+#include "fwd_softmax.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace fa {
 
 namespace {
-
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 
 template <int D>
 struct FwdCfg {
@@ -195,123 +190,30 @@ __global__ void __launch_bounds__(256, 1)
     const int row = wq * 32 + lane;
     const int q = qt * C::BM + row;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
-    float m_run = -INFINITY;  // running max of S * scale * log2(e)
-    float l_run = 0.f;        // running sum of P (for L)
-    float lr_run = 0.f;       // running sum of P as rounded to bf16 for the P V product (for O)
+    SoftmaxRow st;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int b = j % C::NSB;
       if (!(ok = mbar_wait_warp(bar(C::B_SFULL + b), (j / C::NSB) & 1, guard, SITE_FWD_SOFTMAX))) break;
       tc_fence_after();
-      uint32_t r[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tl + C::TM_S0 + b * 128 + 32 * c, r + 32 * c);
-      tmem_ld_wait<128>(r);
-      float s[128];
-#pragma unroll
-      for (int k = 0; k < 128; ++k) s[k] = __uint_as_float(r[k]);
-      const int k0 = (jlo + j) * C::BN;
-      if ((CAUSAL && k0 + C::BN - 1 > qt * C::BM + off) || (WINDOW && k0 <= qt * C::BM + C::BM - 1 + off - window) ||
-          k0 + C::BN > Nk) {
-        // this row sees tile columns lo .. hi (position q + off; keys below Nk)
-        const int hi = min(CAUSAL ? q + off - k0 : C::BN - 1, Nk - 1 - k0);
-        const int lo = WINDOW ? q + off - window + 1 - k0 : 0;
-#pragma unroll
-        for (int k = 0; k < 128; ++k)
-          if (k > hi || k < lo) s[k] = -INFINITY;
-      }
-      // row max as eight independent chains of 3-input maxes (depth ~10, not 127)
-      float m8[8];
-#pragma unroll
-      for (int a = 0; a < 8; ++a) {
-        m8[a] = fmax3(s[16 * a], s[16 * a + 1], s[16 * a + 2]);
-#pragma unroll
-        for (int b = 3; b < 15; b += 2) m8[a] = fmax3(m8[a], s[16 * a + b], s[16 * a + b + 1]);
-        m8[a] = fmaxf(m8[a], s[16 * a + 15]);
-      }
-      const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-      const float m_tile = mx * c_log2;
-      if (j == 0) {
-        m_run = m_tile;
-      } else {
-        const bool move = m_tile > m_run + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, move)) {
-          const float alpha = move ? ex2(m_run - m_tile) : 1.f;
-          if (move) {
-            l_run *= alpha;
-            lr_run *= alpha;
-            m_run = m_tile;
-          }
-          // O holds P_0..P_{j-1} V: wait for the last of those products.  Its barrier
-          // is the one that frees S buffer (j-1) % 3; PV_{j-3} is already done (S_j
-          // waited for it), so that barrier is at most one phase behind.
-          const int pb = (j - 1) % C::NSB;
-          if (!(ok = mbar_wait_warp(bar(C::B_PFREE + pb), ((j - 1) / C::NSB) & 1, guard, SITE_FWD_SOFTMAX))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tl + C::TM_O + 32 * c, o);
-            tmem_ld_wait<32>(o);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tl + C::TM_O + 32 * c, o);
-          }
-          tmem_st_wait();
-        }
-      }
-      // a row whose keys so far were all masked (a window's first tile) keeps
-      // m = -inf; its P is 0 and the first visible tile rescales by 0
-      const float neg_m = (WINDOW && m_run == -INFINITY) ? 0.f : -m_run;
-      // two columns per packed f32x2 instruction: exponent argument, running sums of
-      // P (for L) and of P as rounded to bf16 (for O's normaliser); two chains each
-      const uint64_t cc2 = f2pack(c_log2, c_log2), nm2 = f2pack(neg_m, neg_m);
-      uint64_t ls[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)}, rs[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
-      uint32_t p[64];
-#pragma unroll
-      for (int k = 0; k < 128; k += 2) {
-        float t0, t1;
-        f2unpack(ffma2(f2pack(s[k], s[k + 1]), cc2, nm2), t0, t1);
-        const float p0 = ex2(t0), p1 = ex2(t1);
-        ls[(k >> 1) & 1] = fadd2(ls[(k >> 1) & 1], f2pack(p0, p1));
-        const uint32_t pk = pack_bf16x2(p0, p1);
-        p[k >> 1] = pk;
-        rs[(k >> 1) & 1] = fadd2(rs[(k >> 1) & 1], f2pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
-      }
-      float a0, a1, a2, a3;
-      f2unpack(fadd2(ls[0], ls[1]), a0, a1);
-      f2unpack(fadd2(rs[0], rs[1]), a2, a3);
-      l_run += a0 + a1;
-      lr_run += a2 + a3;
-      tmem_st32(tl + C::TM_S0 + b * 128, p);
-      tmem_st32(tl + C::TM_S0 + b * 128 + 32, p + 32);
-      tmem_st_wait();
+      // O holds P_0..P_{j-1} V: before a rescale, wait for the last of those products.
+      // Its barrier is the one that frees S buffer (j-1) % 3; PV_{j-3} is already done
+      // (S_j waited for it), so that barrier is at most one phase behind.
+      auto wait_o = [&] {
+        const int pb = (j - 1) % C::NSB;
+        return mbar_wait_warp(bar(C::B_PFREE + pb), ((j - 1) / C::NSB) & 1, guard, SITE_FWD_SOFTMAX);
+      };
+      if (!(ok = softmax_tile<D, CAUSAL, WINDOW>(st, tl + C::TM_S0 + b * 128, tl + C::TM_O, j == 0,
+                                                 (jlo + j) * C::BN, qt * C::BM, q, off, Nk, window, c_log2, wait_o)))
+        break;
       tc_fence_before();
       mbar_arrive(bar(C::B_PFULL + b));
     }
     if (ok) ok = mbar_wait_warp(bar(C::B_OFINAL), 0, guard, SITE_FWD_SOFTMAX);
     if (ok) {
       tc_fence_after();
-      // O is normalised by the sum of the very bf16 weights that entered P V, so
-      // that the weights applied to V sum to one; L uses the unrounded sum.
-      const float inv_l = 1.f / lr_run;
-      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * Nq + q) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tl + C::TM_O + 32 * c, o);
-        tmem_ld_wait<32>(o);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (q < Nq) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        }
-      }
-      if (q < Nq) Lout[static_cast<size_t>(bh) * Nq + q] = (m_run + lg2(l_run)) * kLn2;
+      const size_t r0 = static_cast<size_t>(bh) * Nq + q;
+      softmax_epilogue<D>(st, tl + C::TM_O, O + r0 * D, Lout + r0, q < Nq);
     }
   }
 

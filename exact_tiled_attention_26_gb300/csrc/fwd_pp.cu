@@ -19,15 +19,13 @@
 // idle, 4..7 softmax and epilogue of tile A, 8..11 of tile B (one query row per
 // thread, its tensor-memory lane).  Registers move from warpgroup 0 to the two
 // softmax warpgroups with setmaxnreg: 56 + 2 x 224 = 3 x 168.
+#include "fwd_softmax.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace fa {
 
 namespace {
-
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;  // base-2 units, as in fwd.cu
 
 struct PP {
   static constexpr int D = 128, BM = kFwdBr, BN = kFwdBc;
@@ -213,87 +211,17 @@ __global__ void __launch_bounds__(PP::NTHREADS, 1)
       const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
       const uint32_t tS = tl + C::TM_S + 128 * t, tO = tl + C::TM_O + 128 * t;
       const int jlo_t = lo_of(t), n_t = hi_of(t) - jlo_t + 1;
-      float m_run = -INFINITY, l_run = 0.f, lr_run = 0.f;
+      SoftmaxRow st;
       bool ok = true;
       for (int j = 0; j < n_t; ++j) {
         if (!(ok = mbar_wait_warp(bar(C::B_SFULL + t), j & 1, guard, SITE_PP_SOFTMAX))) break;
         tc_fence_after();
-        uint32_t r[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, r + 32 * c);
-        tmem_ld_wait<128>(r);
-        float s[128];
-#pragma unroll
-        for (int k = 0; k < 128; ++k) s[k] = __uint_as_float(r[k]);
-        const int k0 = (jlo_t + j) * C::BN;
-        if ((CAUSAL && k0 + C::BN - 1 > qt * C::BM + off) ||
-            (WINDOW && k0 <= qt * C::BM + C::BM - 1 + off - window) || k0 + C::BN > Nk) {
-          const int hi = min(CAUSAL ? q + off - k0 : C::BN - 1, Nk - 1 - k0);
-          const int lo = WINDOW ? q + off - window + 1 - k0 : 0;
-#pragma unroll
-          for (int k = 0; k < 128; ++k)
-            if (k > hi || k < lo) s[k] = -INFINITY;
-        }
-        float m8[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-          m8[a] = fmax3(s[16 * a], s[16 * a + 1], s[16 * a + 2]);
-#pragma unroll
-          for (int b = 3; b < 15; b += 2) m8[a] = fmax3(m8[a], s[16 * a + b], s[16 * a + b + 1]);
-          m8[a] = fmaxf(m8[a], s[16 * a + 15]);
-        }
-        const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
-        const float m_tile = mx * c_log2;
-        if (j == 0) {
-          m_run = m_tile;
-        } else {
-          const bool move = m_tile > m_run + kRescaleThreshold;
-          if (__any_sync(0xffffffffu, move)) {
-            const float alpha = move ? ex2(m_run - m_tile) : 1.f;
-            if (move) {
-              l_run *= alpha;
-              lr_run *= alpha;
-              m_run = m_tile;
-            }
-            // O_t is at rest: its last product finished before S_t of this tile was formed
-            // (that barrier has completed exactly j phases: the wait returns at once)
-            if (!(ok = mbar_wait_warp(bar(C::B_PFREE + t), (j - 1) & 1, guard, SITE_PP_SOFTMAX))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(tO + 32 * c, o);
-              tmem_ld_wait<32>(o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(tO + 32 * c, o);
-            }
-            tmem_st_wait();
-          }
-        }
-        const float neg_m = (WINDOW && m_run == -INFINITY) ? 0.f : -m_run;
-        const uint64_t cc2 = f2pack(c_log2, c_log2), nm2 = f2pack(neg_m, neg_m);
-        uint64_t ls[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)}, rs[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
-        uint32_t p[64];
-#pragma unroll
-        for (int k = 0; k < 128; k += 2) {
-          float t0, t1;
-          f2unpack(ffma2(f2pack(s[k], s[k + 1]), cc2, nm2), t0, t1);
-          const float p0 = ex2(t0), p1 = ex2(t1);
-          ls[(k >> 1) & 1] = fadd2(ls[(k >> 1) & 1], f2pack(p0, p1));
-          const uint32_t pk = pack_bf16x2(p0, p1);
-          p[k >> 1] = pk;
-          rs[(k >> 1) & 1] =
-              fadd2(rs[(k >> 1) & 1], f2pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
-        }
-        float a0, a1, a2, a3;
-        f2unpack(fadd2(ls[0], ls[1]), a0, a1);
-        f2unpack(fadd2(rs[0], rs[1]), a2, a3);
-        l_run += a0 + a1;
-        lr_run += a2 + a3;
-        tmem_st32(tS, p);
-        tmem_st32(tS + 32, p + 32);
-        tmem_st_wait();
+        // O_t is at rest: its last product finished before S_t of this tile was formed
+        // (that barrier has completed exactly j phases: the wait returns at once)
+        auto wait_o = [&] { return mbar_wait_warp(bar(C::B_PFREE + t), (j - 1) & 1, guard, SITE_PP_SOFTMAX); };
+        if (!(ok = softmax_tile<D, CAUSAL, WINDOW>(st, tS, tO, j == 0, (jlo_t + j) * C::BN, qt * C::BM, q, off, Nk,
+                                                   window, c_log2, wait_o)))
+          break;
         tc_fence_before();
         mbar_arrive(bar(C::B_PFULL + t));
       }
@@ -301,24 +229,8 @@ __global__ void __launch_bounds__(PP::NTHREADS, 1)
       if (ok) ok = mbar_wait_warp(bar(C::B_PFREE + t), (n_t - 1) & 1, guard, SITE_PP_SOFTMAX);
       if (ok) {
         tc_fence_after();
-        const float inv_l = 1.f / lr_run;
-        __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * Nq + q) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * c, o);
-          tmem_ld_wait<32>(o);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (q < Nq) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          }
-        }
-        if (q < Nq) Lout[static_cast<size_t>(bh) * Nq + q] = (m_run + lg2(l_run)) * kLn2;
+        const size_t r0 = static_cast<size_t>(bh) * Nq + q;
+        softmax_epilogue<D>(st, tO, O + r0 * D, Lout + r0, q < Nq);
       }
     }
   }

@@ -1,0 +1,143 @@
+// The forward's per-row softmax work, shared by the one-tile (fwd.cu) and the
+// two-tile (fwd_pp.cu) forward kernels: "CS336 Assignment 2 notes" §1.2 for one
+// query row, one key tile at a time, in base 2 with the softmax scale folded into
+// one FMA.  The thread owns one query row: its tensor-memory lane.
+//
+// The running max is moved lazily: only when a row's max grows by more than 8
+// (base 2) is it moved and O, l multiplied by 2^(m_old - m_new).  Between moves
+// P <= 2^8, well inside fp32 and bf16 range; O / l does not depend on which
+// reference max was used.
+#pragma once
+
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr float kFwdRescaleThreshold = 8.0f;  // base-2 units
+constexpr float kFwdLn2 = 0.6931471805599453f;
+
+// Running state of one query row.
+struct SoftmaxRow {
+  float m_run = -INFINITY;  // running (reference) max of S * scale * log2(e)
+  float l_run = 0.f;        // running sum of P (for L)
+  float lr_run = 0.f;       // running sum of P as rounded to bf16 for the P V product (for O)
+};
+
+// One 128-key tile for the calling thread's query row q: S (128 fp32 columns at
+// tS, already complete) is masked, the running max updated, and P = 2^(S c - m)
+// written back as bf16 over the first 64 columns at tS (the tensor-memory stores
+// are complete on return).  When the max moves, O (D columns at tO) is rescaled
+// after wait_o() reports that the product that last wrote O is complete.
+//   first: the row's first key tile; k0: its first key; row0: first query row of
+//   the query tile (for the edge test); off = Nk - Nq (query q sits at q + off).
+// Returns false only if wait_o() gave up.
+template <int D, bool CAUSAL, bool WINDOW, class WaitO>
+FA_DEV bool softmax_tile(SoftmaxRow& st, uint32_t tS, uint32_t tO, bool first, int k0, int row0, int q, int off,
+                         int Nk, int window, float c_log2, WaitO&& wait_o) {
+  constexpr int BM = 128, BN = 128;
+  uint32_t r[128];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, r + 32 * c);
+  tmem_ld_wait<128>(r);
+  float s[128];
+#pragma unroll
+  for (int k = 0; k < 128; ++k) s[k] = __uint_as_float(r[k]);
+  if ((CAUSAL && k0 + BN - 1 > row0 + off) || (WINDOW && k0 <= row0 + BM - 1 + off - window) || k0 + BN > Nk) {
+    // this row sees tile columns lo .. hi (position q + off; keys below Nk)
+    const int hi = min(CAUSAL ? q + off - k0 : BN - 1, Nk - 1 - k0);
+    const int lo = WINDOW ? q + off - window + 1 - k0 : 0;
+#pragma unroll
+    for (int k = 0; k < 128; ++k)
+      if (k > hi || k < lo) s[k] = -INFINITY;
+  }
+  // row max as eight independent chains of 3-input maxes (depth ~10, not 127)
+  float m8[8];
+#pragma unroll
+  for (int a = 0; a < 8; ++a) {
+    m8[a] = fmax3(s[16 * a], s[16 * a + 1], s[16 * a + 2]);
+#pragma unroll
+    for (int b = 3; b < 15; b += 2) m8[a] = fmax3(m8[a], s[16 * a + b], s[16 * a + b + 1]);
+    m8[a] = fmaxf(m8[a], s[16 * a + 15]);
+  }
+  const float mx = fmax3(fmax3(m8[0], m8[1], m8[2]), fmax3(m8[3], m8[4], m8[5]), fmaxf(m8[6], m8[7]));
+  const float m_tile = mx * c_log2;
+  if (first) {
+    st.m_run = m_tile;
+  } else {
+    const bool move = m_tile > st.m_run + kFwdRescaleThreshold;
+    if (__any_sync(0xffffffffu, move)) {
+      const float alpha = move ? ex2(st.m_run - m_tile) : 1.f;
+      if (move) {
+        st.l_run *= alpha;
+        st.lr_run *= alpha;
+        st.m_run = m_tile;
+      }
+      if (!wait_o()) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * c, o);
+        tmem_ld_wait<32>(o);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(tO + 32 * c, o);
+      }
+      tmem_st_wait();
+    }
+  }
+  // a row whose keys so far were all masked (a window's first tile) keeps
+  // m = -inf; its P is 0 and the first visible tile rescales by 0
+  const float neg_m = (WINDOW && st.m_run == -INFINITY) ? 0.f : -st.m_run;
+  // two columns per packed f32x2 instruction: exponent argument, running sums of
+  // P (for L) and of P as rounded to bf16 (for O's normaliser); two chains each
+  const uint64_t cc2 = f2pack(c_log2, c_log2), nm2 = f2pack(neg_m, neg_m);
+  uint64_t ls[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)}, rs[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+  uint32_t p[64];
+#pragma unroll
+  for (int k = 0; k < 128; k += 2) {
+    float t0, t1;
+    f2unpack(ffma2(f2pack(s[k], s[k + 1]), cc2, nm2), t0, t1);
+    const float p0 = ex2(t0), p1 = ex2(t1);
+    ls[(k >> 1) & 1] = fadd2(ls[(k >> 1) & 1], f2pack(p0, p1));
+    const uint32_t pk = pack_bf16x2(p0, p1);
+    p[k >> 1] = pk;
+    rs[(k >> 1) & 1] = fadd2(rs[(k >> 1) & 1], f2pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
+  }
+  float a0, a1, a2, a3;
+  f2unpack(fadd2(ls[0], ls[1]), a0, a1);
+  f2unpack(fadd2(rs[0], rs[1]), a2, a3);
+  st.l_run += a0 + a1;
+  st.lr_run += a2 + a3;
+  tmem_st32(tS, p);
+  tmem_st32(tS + 32, p + 32);
+  tmem_st_wait();
+  return true;
+}
+
+// Epilogue of one query row once every P V product into O (at tO) is complete:
+// O / l to bf16 (l = the sum of the very bf16 weights that entered P V, so that the
+// weights applied to V sum to one) and L = m + ln l with the unrounded sum.  Rows
+// at or past Nq compute but store nothing.
+template <int D>
+FA_DEV void softmax_epilogue(const SoftmaxRow& st, uint32_t tO, __nv_bfloat16* orow, float* lrow, bool store) {
+  const float inv_l = 1.f / st.lr_run;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tO + 32 * c, o);
+    tmem_ld_wait<32>(o);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+    if (store) {
+      uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+  }
+  if (store) *lrow = (st.m_run + lg2(st.l_run)) * kFwdLn2;
+}
+
+}  // namespace fa
