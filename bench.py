@@ -296,8 +296,11 @@ def run_ours(args):
     w = si.WORKLOADS[args.workload]
     causal = True if len(w.causal) == 1 and w.causal[0] else (args.causal if args.causal is not None else w.causal[-1])
     fa.check(fa.fa_debug_set_bwd_split(args.bwd_split), "fa_debug_set_bwd_split")
-    r = Runner(fa, torch, w, causal, dev)
+    r = Runner(fa, torch, w, causal, dev, window=args.window)
     flops_f, flops_b = w.fwd_flops(causal), w.bwd_flops(causal)
+    if args.window:  # FLOPs on the visible entries only
+        flops_f = 4.0 * w.d * w.B * w.H * r.visible_pairs()
+        flops_b = 2.5 * flops_f
 
     # warm-up (also compiles nothing: the library is prebuilt), then the timed region
     for _ in range(args.warmup):
@@ -334,13 +337,15 @@ def run_ours(args):
             "kernel": "bwd_d128_kernel (timed as the fa_bwd call: main kernel + workspace clear + dQ convert)",
             "achieved": round(bwd_tflops, 2), "peak": sustained, "unit": "TFLOP/s",
             "frac": round(bwd_tflops / sustained, 4),
-            "traffic": _TRAFFIC.get((w.name, causal)),
+            "traffic": None if args.window else _TRAFFIC.get((w.name, causal)),
             "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside back-to-back steps)",
             "algorithmic": "10 N^2 d / 2 FLOPs per head (causal) per launch",
         },
         "gpu_launches": Runner.LAUNCHES_PER_STEP * args.steps,
         "clocks": clk.summary(),
     }
+    if args.window:
+        line["config"]["window"] = args.window
     if not args.quick and rank == 0:
         # end to end through the C ABI with host buffers
         steps_e2e = max(2, min(args.steps, 5))
@@ -462,9 +467,14 @@ def main():
     ap.add_argument("--quick", action="store_true", help="headline timing only (for profiler runs)")
     ap.add_argument("--bwd-split", type=int, default=0, choices=[0, 1, 2],
                     help="backward form for d=128: 1 one kernel + dQ reduction, 2 two kernels, 0 library default")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window over the workload's causal mask (with --quick: profiler runs of the "
+                         "windowed kernels)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.quick:
         ap.error("at least 3 warm-up steps")
+    if args.window and (not args.quick or args.impl != "ours"):
+        ap.error("--window is for --quick runs of this library")
     if args.impl == "reference":
         run_reference(args)
     else:
