@@ -286,6 +286,15 @@ def test_causal_fraction_table():
         assert pairs / total == pytest.approx(0.5 + 0.5 / T, rel=1e-15)
 
 
+def test_tiny_case_tile_count_at_64_tiles():
+    """The tiny case (N = 256) at the 64 x 64 tiles it is written for: 4 tile rows,
+    so 4 * 5 / 2 = 10 of the 16 pairs are computed with the causal mask.  The GPU
+    runs 128 x 128 tiles there; this count is pinned on the CPU tiled oracle."""
+    Q, K, V = (_rand(95 + i, 256, 32) for i in range(3))
+    assert oracle.flash_forward_tiled(Q, K, V, 64, 64, True)[2] == oracle.causal_tile_pairs(256, 64, 64, True) == 10
+    assert oracle.flash_forward_tiled(Q, K, V, 64, 64, False)[2] == oracle.causal_tile_pairs(256, 64, 64, False) == 16
+
+
 def test_flop_count():
     # 12 N^2 d standard vs 14 N^2 d recompute for N = 1024, d = 64 (805.3 M vs 939.5 M)
     f, b = oracle.attention_flops(1024, 64, False)
