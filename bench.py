@@ -355,7 +355,8 @@ def run_ours(args):
         line["e2e"] = {"value": round((flops_f + flops_b) * steps_e2e / (ms / 1e3) / 1e12, 2), "unit": UNIT,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "ms_per_step": round(ms / steps_e2e, 3),
-                       "api": f"fa_fwd_bwd_host (pinned host arrays; {hc} heads per chunk, copies overlapped)",
+                       "api": f"fa_fwd_bwd_host (pinned host arrays; {hc} head{'s' if hc != 1 else ''} per chunk, "
+                              "copies overlapped)",
                        "serial_ms_per_step": round(ms_serial / steps_e2e, 3)}
         line["per_config"] = per_config(fa, torch, dev, peaks)
         line["cpu_baseline"] = cpu_oracle_sample(w, causal)

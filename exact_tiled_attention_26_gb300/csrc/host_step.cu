@@ -15,8 +15,11 @@ namespace {
 
 constexpr int kSlots = 4;           // chunks whose device copies are live at once
 constexpr int kComputeStreams = 2;  // chunks computed alternately on two streams
-constexpr int kTargetChunks = 8;    // enough chunks that the first copy in and last copy out are short
-constexpr int kMinTilesPerChunk = 2 * 152;  // two waves of the 152 SMs per launch
+// Small chunks keep the first copy in and the last copy out short; each launch
+// should still fill the 152 SMs once.  Measured on the 1 x 32 x 32768 x 128 causal
+// step: 1, 2, 4 and 8 heads per chunk gave about 1170, 1156, 1128 and 1077 TFLOP/s.
+constexpr int kTargetChunks = 32;
+constexpr int kMinTilesPerChunk = 152;
 constexpr int kMaxDevices = 64;
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -59,8 +62,7 @@ struct Plan {
 int chunk_heads(int BH, int Nq, int Nk, int heads_per_chunk) {
   if (BH <= 0) return 0;
   if (heads_per_chunk > 0) return heads_per_chunk < BH ? heads_per_chunk : BH;
-  // each launch should still fill the GPU a few times over: at least two waves of
-  // tiles per chunk, in the shorter of the query and key directions
+  // at least one wave of tiles per chunk, in the shorter of the query and key directions
   const int tq = (Nq + kFwdBr - 1) / kFwdBr, tk = (Nk + kBwdBc - 1) / kBwdBc;
   const int tiles = (tq < tk ? tq : tk) > 0 ? (tq < tk ? tq : tk) : 1;
   int hc = (kMinTilesPerChunk + tiles - 1) / tiles;
@@ -88,7 +90,9 @@ Plan make_plan(int BH, int Nq, int Nk, int d, int causal, int window, int heads_
 struct Pipe {
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr, comp[kComputeStreams] = {};
-  cudaEvent_t start = nullptr, end = nullptr, in[kSlots] = {}, done[kSlots] = {}, out[kSlots] = {};
+  // per slot: Q, K, V in; dO in; forward done (O, L ready); backward done; every output out
+  cudaEvent_t start = nullptr, end = nullptr, in_qkv[kSlots] = {}, in[kSlots] = {}, fwd[kSlots] = {}, done[kSlots] = {},
+              out[kSlots] = {};
 };
 Pipe g_pipe[kMaxDevices];
 std::mutex g_pipe_mu;  // held for a whole enqueue: the slot events are shared
@@ -100,7 +104,8 @@ bool make_pipe(Pipe* p) {
   auto event = [](cudaEvent_t* e) { return *e != nullptr || cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
   bool ok = stream(&p->h2d) && stream(&p->d2h) && event(&p->start) && event(&p->end);
   for (int i = 0; ok && i < kComputeStreams; ++i) ok = stream(&p->comp[i]);
-  for (int i = 0; ok && i < kSlots; ++i) ok = event(&p->in[i]) && event(&p->done[i]) && event(&p->out[i]);
+  for (int i = 0; ok && i < kSlots; ++i)
+    ok = event(&p->in_qkv[i]) && event(&p->in[i]) && event(&p->fwd[i]) && event(&p->done[i]) && event(&p->out[i]);
   p->ready = ok;
   return ok;
 }
@@ -177,21 +182,26 @@ fa_status fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const voi
     char* sb = ws + p.slot.bytes * slot;
     const size_t bq = nq * 2 * hn, bk = nk * 2 * hn, bl = static_cast<size_t>(Nq) * 4 * hn;
     const size_t off_q = nq * 2 * h0, off_k = nk * 2 * h0, off_l = static_cast<size_t>(Nq) * 4 * h0;
-    // in: this slot's inputs were last read by the chunk `slots` earlier
+    // in: this slot's inputs were last read by the chunk `slots` earlier.  Q, K, V
+    // first (the forward needs only those), then dO.
     ok = (c < p.slots || cudaStreamWaitEvent(pp.h2d, pp.done[slot], 0) == cudaSuccess) &&
          copy(sb + p.slot.q, hQ + off_q, bq, cudaMemcpyHostToDevice, pp.h2d) &&
          copy(sb + p.slot.k, hK + off_k, bk, cudaMemcpyHostToDevice, pp.h2d) &&
          copy(sb + p.slot.v, hV + off_k, bk, cudaMemcpyHostToDevice, pp.h2d) &&
+         cudaEventRecord(pp.in_qkv[slot], pp.h2d) == cudaSuccess &&
          copy(sb + p.slot.dO, hdO + off_q, bq, cudaMemcpyHostToDevice, pp.h2d) &&
          cudaEventRecord(pp.in[slot], pp.h2d) == cudaSuccess;
     if (!ok) return FA_ERR_CUDA;
-    // compute: after the inputs arrived and the slot's previous outputs left
-    if (cudaStreamWaitEvent(cs, pp.in[slot], 0) != cudaSuccess ||
+    // compute: the forward after Q, K, V arrived and the slot's previous outputs
+    // left; the backward after dO arrived
+    if (cudaStreamWaitEvent(cs, pp.in_qkv[slot], 0) != cudaSuccess ||
         (c >= p.slots && cudaStreamWaitEvent(cs, pp.out[slot], 0) != cudaSuccess))
       return FA_ERR_CUDA;
     st = fa_fwd_ex(sb + p.slot.q, sb + p.slot.k, sb + p.slot.v, sb + p.slot.o, reinterpret_cast<float*>(sb + p.slot.L),
                    1, hn, Nq, Nk, d, causal, window, scale, cs);
     if (st != FA_OK) return st;
+    if (cudaEventRecord(pp.fwd[slot], cs) != cudaSuccess || cudaStreamWaitEvent(cs, pp.in[slot], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
     st = fa_bwd_preprocess(sb + p.slot.o, sb + p.slot.dO, reinterpret_cast<float*>(sb + p.slot.D), 1, hn, Nq, d, cs);
     if (st != FA_OK) return st;
     st = fa_bwd_ex(sb + p.slot.q, sb + p.slot.k, sb + p.slot.v, sb + p.slot.o, sb + p.slot.dO,
@@ -200,10 +210,11 @@ fa_status fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const voi
                    acc + p.acc_bytes * (c % p.streams), p.acc_bytes, cs);
     if (st != FA_OK) return st;
     if (cudaEventRecord(pp.done[slot], cs) != cudaSuccess) return FA_ERR_CUDA;
-    // out
-    ok = cudaStreamWaitEvent(pp.d2h, pp.done[slot], 0) == cudaSuccess &&
+    // out: O and L once the forward is done, the gradients once the backward is
+    ok = cudaStreamWaitEvent(pp.d2h, pp.fwd[slot], 0) == cudaSuccess &&
          copy(hO + off_q, sb + p.slot.o, bq, cudaMemcpyDeviceToHost, pp.d2h) &&
          copy(hL + off_l, sb + p.slot.L, bl, cudaMemcpyDeviceToHost, pp.d2h) &&
+         cudaStreamWaitEvent(pp.d2h, pp.done[slot], 0) == cudaSuccess &&
          copy(hdQ + off_q, sb + p.slot.dQ, bq, cudaMemcpyDeviceToHost, pp.d2h) &&
          copy(hdK + off_k, sb + p.slot.dK, bk, cudaMemcpyDeviceToHost, pp.d2h) &&
          copy(hdV + off_k, sb + p.slot.dV, bk, cudaMemcpyDeviceToHost, pp.d2h) &&

@@ -16,16 +16,17 @@ def _tiles(n):
 
 @pytest.mark.parametrize("B,H,Nq,Nk,d", SHAPES)
 def test_automatic_chunks(fa_lib, B, H, Nq, Nk, d):
-    """Each chunk keeps at least one wave of 128-row tiles on the 152 SMs (or is the
-    whole batch), there are at most 8 chunks, and chunks are even (the last one short
-    by fewer heads than there are chunks)."""
+    """Each chunk keeps at least half a wave of 128-row tiles on the 152 SMs (one
+    wave before the chunks are evened out), or is the whole batch; there are at most
+    32 chunks, and chunks are even (the last one short by fewer heads than there are
+    chunks)."""
     BH = B * H
     hc = fa_lib.fa_fwd_bwd_host_chunk_heads(B, H, Nq, Nk, d, 0)
     assert 1 <= hc <= BH
     chunks = math.ceil(BH / hc)
-    assert chunks <= 8
+    assert chunks <= 32
     assert hc * chunks - BH < chunks
-    assert hc == BH or hc * min(_tiles(Nq), _tiles(Nk)) >= 152
+    assert hc == BH or hc * min(_tiles(Nq), _tiles(Nk)) >= 76
 
 
 def test_chunk_override_and_errors(fa_lib):
