@@ -23,6 +23,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -56,6 +57,8 @@ def _peaks():
 # ------------------------------------------------------------------ clocks sampling
 
 class ClockSampler:
+    """nvidia-smi samples of the SM clock, power and throttle reasons during the timed
+    region; the raw samples go to $FA_CLOCKS_DIR (default: the temporary directory)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -63,7 +66,7 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(os.environ.get("FA_CLOCKS_DIR") or tempfile.gettempdir(), f"fa_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
