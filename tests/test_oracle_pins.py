@@ -23,7 +23,7 @@ def _rand(seed, *shape):
 
 
 def _torch_reference(Q, K, V, dO, causal, scale):
-    """torch fp64 autograd through softmax(Q K^T s) V: an independent library judge
+    """torch fp64 autograd through softmax(Q K^T s) V: an independent library check
     (the cross-check of the CS324 lecture 8 script, demo4_backward)."""
     tq, tk, tv = (torch.tensor(a, requires_grad=True) for a in (Q, K, V))
     s = tq @ tk.transpose(-2, -1) * scale
