@@ -194,7 +194,8 @@ def e2e_steps(torch, r: Runner, steps: int, pipelined: bool = True):
     pinned host -> device copies of Q, K, V, dO and device -> pinned host copies of O,
     L, dQ, dK, dV inside the timed region.  pipelined: one fa_fwd_bwd_host call
     per step (heads in chunks, copies overlapped with the kernels); otherwise the
-    copies and the three device calls one after another on one stream."""
+    copies and the three device calls one after another on one stream.  Returns the
+    median milliseconds of three blocks of `steps` steps."""
     fa, w = r.fa, r.w
     outs = [r.o, r.lse, r.dq, r.dk, r.dv]
     host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
@@ -220,14 +221,19 @@ def e2e_steps(torch, r: Runner, steps: int, pipelined: bool = True):
 
     step()  # warm-up: creates the library's copy streams
     torch.cuda.synchronize()
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(r.stream)
-    for _ in range(steps):
-        step()
-    stop.record(r.stream)
-    torch.cuda.synchronize()
+    # three blocks of `steps` steps; the median block (host memory traffic from other
+    # processes on the machine can slow a single block)
+    blocks = []
+    for _ in range(3):
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(r.stream)
+        for _ in range(steps):
+            step()
+        stop.record(r.stream)
+        torch.cuda.synchronize()
+        blocks.append(start.elapsed_time(stop))
     del ws
-    return start.elapsed_time(stop), h2d, d2h
+    return statistics.median(blocks), h2d, d2h
 
 
 def cpu_oracle_sample(w: si.Workload, causal: bool, budget_s: float = 12.0, max_rows=None):

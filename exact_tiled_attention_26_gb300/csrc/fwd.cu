@@ -62,7 +62,8 @@ template <int D, int MASK>
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ Lout,
-               int Nq, int Nk, int window, float c_log2, int* status, unsigned long long* tile_counter) {
+               int Nq, int Nk, int window, float c_log2, int* status, unsigned long long* tile_counter,
+               int head_group) {
   using C = FwdCfg<D>;
   constexpr bool CAUSAL = MASK >= 1, WINDOW = MASK == 2;
   extern __shared__ uint8_t smem_raw[];
@@ -75,8 +76,9 @@ __global__ void __launch_bounds__(256, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = (Nq + C::BM - 1) / C::BM;
-  const int qt = T - 1 - static_cast<int>(blockIdx.x);  // longest causal rows first
-  const int bh = blockIdx.y;
+  int qt = 0, bh = 0;  // longest causal rows first, heads in groups (grouped_tile_head)
+  grouped_tile_head(blockIdx.y * gridDim.x + blockIdx.x, T, gridDim.y, head_group, &qt, &bh);
+  qt = T - 1 - qt;
   const int off = Nk - Nq;  // position of query row i is i + off
   // visible key tiles jlo .. jlo + n_kv - 1 (whole-tile skip on both sides of the band)
   int jlo = 0, jhi = 0;
@@ -246,7 +248,7 @@ fa_status launch_fwd_t(const FwdLaunch& a) {
   const dim3 grid((a.Nq + C::BM - 1) / C::BM, a.BH);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   kern<<<grid, 256, C::SMEM, a.stream>>>(mQ, mK, mV, static_cast<__nv_bfloat16*>(a.O), a.L, a.Nq, a.Nk, a.window,
-                                         c_log2, a.status, a.counter);
+                                         c_log2, a.status, a.counter, head_group(a.BH, a.Nq, a.Nk, D));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -50,7 +50,8 @@ template <int MASK>
 __global__ void __launch_bounds__(PP::NTHREADS, 1)
     fwd_pp_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O, float* __restrict__ Lout,
-                  int Nq, int Nk, int window, float c_log2, int* status, unsigned long long* tile_counter) {
+                  int Nq, int Nk, int window, float c_log2, int* status, unsigned long long* tile_counter,
+                  int head_group) {
   using C = PP;
   constexpr bool CAUSAL = MASK >= 1, WINDOW = MASK == 2;
   constexpr int D = C::D;
@@ -65,8 +66,9 @@ __global__ void __launch_bounds__(PP::NTHREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = (Nq + C::BM - 1) / C::BM;     // query tiles
   const int npair = (T + 1) / 2;
-  const int qp = npair - 1 - static_cast<int>(blockIdx.x);  // longest causal rows first
-  const int bh = blockIdx.y;
+  int qp = 0, bh = 0;  // longest causal rows first, heads in groups (grouped_tile_head)
+  grouped_tile_head(blockIdx.y * gridDim.x + blockIdx.x, npair, gridDim.y, head_group, &qp, &bh);
+  qp = npair - 1 - qp;
   const int off = Nk - Nq;
   const int w = WINDOW ? window : 0;
   // visible key tiles of each query tile; tile B may not exist (odd T)
@@ -264,7 +266,8 @@ fa_status launch_pp_t(const FwdLaunch& a) {
   const dim3 grid((T + 1) / 2, a.BH);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   kern<<<grid, C::NTHREADS, C::SMEM, a.stream>>>(mQ, mK, mV, static_cast<__nv_bfloat16*>(a.O), a.L, a.Nq, a.Nk,
-                                                 a.window, c_log2, a.status, a.counter);
+                                                 a.window, c_log2, a.status, a.counter,
+                                                 head_group(a.BH, a.Nq, a.Nk, C::D));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
