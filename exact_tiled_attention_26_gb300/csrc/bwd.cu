@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(256, 1)
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                const float* __restrict__ Lg, const float* __restrict__ Dg, float* __restrict__ dQacc,
                __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int Nq, int Nk, int window, float c_log2, float scale,
-               int* status, unsigned long long* tile_counter) {
+               int* status, unsigned long long* tile_counter, int head_group) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
@@ -86,8 +86,8 @@ __global__ void __launch_bounds__(256, 1)
   const Guard guard{status, abort_flag};
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kt = blockIdx.x;  // key tile; the longest causal loops come first
-  const int bh = blockIdx.y;
+  int kt = 0, bh = 0;  // key tile (the longest causal loops first) and head, heads in groups (grouped_tile_head)
+  grouped_tile_head(blockIdx.y * gridDim.x + blockIdx.x, gridDim.x, gridDim.y, head_group, &kt, &bh);
   const int off = Nk - Nq;  // position of query row i is i + off
   // visible query tiles i0 .. i0 + n_it - 1 (none: this CTA writes zero dK, dV)
   int i0 = 0, ilast = 0;
@@ -373,7 +373,7 @@ fa_status launch_bwd_t(const BwdLaunch& a) {
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   kern<<<grid, 256, C::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D, a.dQacc, static_cast<__nv_bfloat16*>(a.dK),
                                          static_cast<__nv_bfloat16*>(a.dV), a.Nq, a.Nk, a.window, c_log2, a.scale, a.status,
-                                         a.counter);
+                                         a.counter, head_group(a.BH, a.Nq, a.Nk, D));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(KVC<D>::NTHREADS, 1)
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const float* __restrict__ Lg, const float* __restrict__ Dg, __nv_bfloat16* __restrict__ dK,
                   __nv_bfloat16* __restrict__ dV, int Nq, int Nk, int window, float c_log2, float scale, int* status,
-                  unsigned long long* tile_counter) {
+                  unsigned long long* tile_counter, int head_group) {
   using C = KVC<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw + C::SMALL);
@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(KVC<D>::NTHREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + C::OFF_MISC + 4);
   const Guard guard{status, abort_flag};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kt = blockIdx.x, bh = blockIdx.y;
+  int kt = 0, bh = 0;  // longest causal loops first, heads in groups (grouped_tile_head)
+  grouped_tile_head(blockIdx.y * gridDim.x + blockIdx.x, gridDim.x, gridDim.y, head_group, &kt, &bh);
   const int off = Nk - Nq;  // position of query row i is i + off
   int i0 = 0, ilast = 0;
   query_tile_range(kt, 128, 128, Nq, Nk, CAUSAL, window, &i0, &ilast);
@@ -359,7 +360,7 @@ __global__ void __launch_bounds__(QC<D>::NTHREADS, 1)
     bwd_q_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                  const float* __restrict__ Lg, const float* __restrict__ Dg, __nv_bfloat16* __restrict__ dQ, int Nq, int Nk, int window,
-                 float c_log2, float scale, int* status) {
+                 float c_log2, float scale, int* status, int head_group) {
   using C = QC<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw + C::SMALL);
@@ -370,8 +371,9 @@ __global__ void __launch_bounds__(QC<D>::NTHREADS, 1)
   const Guard guard{status, abort_flag};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = (Nq + 127) / 128;
-  const int qt = T - 1 - static_cast<int>(blockIdx.x);  // longest causal rows first
-  const int bh = blockIdx.y;
+  int qt = 0, bh = 0;  // longest causal rows first, heads in groups (grouped_tile_head)
+  grouped_tile_head(blockIdx.y * gridDim.x + blockIdx.x, T, gridDim.y, head_group, &qt, &bh);
+  qt = T - 1 - qt;
   const int off = Nk - Nq;
   int jlo = 0, jhi = 0;  // visible key tiles (every query row sees at least one key)
   key_tile_range(qt, 128, 128, Nq, Nk, CAUSAL, window, &jlo, &jhi);
@@ -599,11 +601,12 @@ fa_status launch_t(const BwdLaunch& a, void* dQ) {
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   kkv<<<dim3(Tk, a.BH), KVC<D>::NTHREADS, KVC<D>::SMEM, a.stream>>>(
       mQ, mK, mV, mdO, a.L, a.D, static_cast<__nv_bfloat16*>(a.dK), static_cast<__nv_bfloat16*>(a.dV), a.Nq, a.Nk,
-      a.window, c_log2, a.scale, a.status, a.counter);
+      a.window, c_log2, a.scale, a.status, a.counter, head_group(a.BH, a.Nq, a.Nk, D));
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   kq<<<dim3(Tq, a.BH), QC<D>::NTHREADS, QC<D>::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D,
                                                            static_cast<__nv_bfloat16*>(dQ), a.Nq, a.Nk, a.window,
-                                                           c_log2, a.scale, a.status);
+                                                           c_log2, a.scale, a.status,
+                                                           head_group(a.BH, a.Nq, a.Nk, D));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
