@@ -42,7 +42,7 @@ UNIT = "TFLOP/s"
 # backward main kernel, from the ncu capture summarised in
 # profiles/launches_vlong_1x32x32768x128_causal.md; valid for the kernel as captured
 # there (set to None whenever the kernel changes).
-_TRAFFIC = {("vlong_1x32x32768x128", True): 1620219136 + 1022620928}
+_TRAFFIC = {("vlong_1x32x32768x128", True): 1620360448 + 1022791424}
 
 
 def _peaks():
