@@ -189,23 +189,25 @@ fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter) {
   return FA_OK;
 }
 
-// Which forward kernel runs.  Measured on GB300: two query tiles per CTA (form 2)
-// is faster when every query tile sees at most 16 key tiles (short windows,
-// sequences up to 2048: +1% to +21%), the one-tile form with its deeper S buffering
-// when query tiles see more (up to 14% faster at 32 key tiles), and with fewer than
-// two query tiles per head form 2 has nothing to pair.
+// Which forward kernel runs (fa_debug_set_fwd_form overrides).  Measured on GB300,
+// forward TFLOP/s: the persistent kernel (form 3) hides most of the fixed cost of a
+// CTA and wins whenever query tiles see few key tiles, e.g. at d = 128 the 1024-key
+// window on 1 x 32 x 8192 763 against 689 (one tile per CTA) and 732 (two tiles per
+// CTA), 8 x 16 x 2048 causal 887 against 804 and 840, 2 x 16 x 4096 causal 1035
+// against 1007, and at d = 64 every shape measured (2 x 16 x 4096 causal 628 against
+// 586); with long key ranges at d = 128 (1 x 32 x 32768 causal, a 2048-query prefill
+// chunk of 32768 keys) the one-tile kernel is 2-3% faster.
 static int fwd_form(int d, int Nq, int Nk, bool causal, int window) {
-  if (d != 128) return 1;
-  if (g_fwd_form != 0) return g_fwd_form;
+  if (g_fwd_form != 0) return (g_fwd_form == 2 && d != 128) ? 1 : g_fwd_form;
+  if (d != 128) return 3;
   const int T = (Nq + kFwdBr - 1) / kFwdBr;
-  if (T < 2) return 1;
   for (int qt = T - 1; qt >= 0; --qt) {  // the widest ranges are at the end (causal) or inside (window)
     int lo = 0, hi = -1;
     key_tile_range(qt, kFwdBr, kFwdBc, Nq, Nk, causal, window, &lo, &hi);
-    if (hi - lo + 1 > 16) return 1;
+    if (hi - lo + 1 > 48) return 1;
     if (window == 0) break;  // without a window the last query tile sees the most
   }
-  return 2;
+  return 3;
 }
 
 fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int Nq, int Nk,
@@ -221,7 +223,8 @@ fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float*
   int* status = device_status_word();
   if (status == nullptr) return FA_ERR_CUDA;
   FwdLaunch a{Q, K, V, O, L, B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
-  return fwd_form(d, Nq, Nk, causal != 0, window) == 2 ? launch_fwd_pp(a) : launch_fwd(a);
+  const int form = fwd_form(d, Nq, Nk, causal != 0, window);
+  return form == 2 ? launch_fwd_pp(a) : form == 3 ? launch_fwd_persist(a) : launch_fwd(a);
 }
 
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
@@ -260,7 +263,7 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
 }
 
 fa_status fa_debug_set_fwd_form(int form) {
-  if (form < 0 || form > 2) return FA_ERR_INVALID_ARG;
+  if (form < 0 || form > 3) return FA_ERR_INVALID_ARG;
   g_fwd_form = form;
   return FA_OK;
 }

@@ -140,4 +140,29 @@ FA_DEV void softmax_epilogue(const SoftmaxRow& st, uint32_t tO, __nv_bfloat16* o
   if (store) *lrow = (st.m_run + lg2(st.l_run)) * kFwdLn2;
 }
 
+// The epilogue in two halves, for a caller that must release O's columns before the
+// global stores: load O / l into packed bf16 registers (the tensor-memory loads are
+// complete on return), then store them and L.
+template <int D>
+FA_DEV void softmax_epilogue_load(const SoftmaxRow& st, uint32_t tO, uint32_t (&pk)[D / 2]) {
+  const float inv_l = 1.f / st.lr_run;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tO + 32 * c, o);
+    tmem_ld_wait<32>(o);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[16 * c + i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+  }
+}
+template <int D>
+FA_DEV void softmax_epilogue_store(const SoftmaxRow& st, const uint32_t (&pk)[D / 2], __nv_bfloat16* orow,
+                                   float* lrow) {
+  uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+  *lrow = (st.m_run + lg2(st.l_run)) * kFwdLn2;
+}
+
 }  // namespace fa

@@ -109,6 +109,8 @@ struct FwdLaunch {
 fa_status launch_fwd(const FwdLaunch& a);
 // d = 128 forward with two query tiles per CTA (fwd_pp.cu).
 fa_status launch_fwd_pp(const FwdLaunch& a);
+// Forward with one CTA per SM taking work units from a queue (fwd_persist.cu).
+fa_status launch_fwd_persist(const FwdLaunch& a);
 
 struct BwdLaunch {
   const void *Q, *K, *V, *dO;

@@ -260,12 +260,17 @@ fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter);
 fa_status fa_debug_set_bwd_split(int split);
 
 /*
- * Debug: which forward kernel fa_fwd runs for d = 128 (the same computation,
- * "CS336 Assignment 2 notes" §1.2; other d always run form 1):
+ * Debug: which forward kernel fa_fwd runs (the same computation, "CS336
+ * Assignment 2 notes" §1.2; form 2 exists for d = 128 only, other d run form 1
+ * in its place):
  *   1: one 128-row query tile per CTA;
  *   2: two query tiles per CTA whose softmax and tensor-core work take turns;
- *   0: the library's default, chosen by measurement on GB300: form 2 when there
- *      are at least two query tiles and none sees more than 16 key tiles, else 1.
+ *   3: one CTA per SM taking query tiles from a queue, consecutive tiles
+ *      overlapped (any d).  Each launch takes the next of 1024 work counters in
+ *      a static device array (no allocation) and zeroes it on its stream; at
+ *      most 1024 such launches may be in flight at once across streams;
+ *   0: the library's default, chosen by measurement on GB300: form 3 for d <= 64,
+ *      and for d = 128 when no query tile sees more than 48 key tiles; else 1.
  * Process-wide setting; FA_ERR_INVALID_ARG for other values.
  */
 fa_status fa_debug_set_fwd_form(int form);

@@ -167,7 +167,7 @@ def test_masked_argument_errors(fa_lib):
 
 def test_forward_form_switch(fa_lib):
     fa = fa_lib
-    for form in (0, 1, 2, 0):
+    for form in (0, 1, 2, 3, 0):
         assert fa.fa_debug_set_fwd_form(form) == fa.FA_OK
-    assert fa.fa_debug_set_fwd_form(3) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_set_fwd_form(4) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_debug_set_fwd_form(-1) == fa.FA_ERR_INVALID_ARG

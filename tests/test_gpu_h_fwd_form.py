@@ -1,8 +1,9 @@
-"""The two d = 128 forward kernels (fa_debug_set_fwd_form: 1 one query tile per
-CTA, 2 two query tiles per CTA taking turns on the tensor pipe) run the same
-arithmetic on each row in the same order, so O and L must agree bit for bit;
-form 2 is also checked against the float64 oracle, over masks, ragged and odd
-tile counts (a last CTA with one query tile), N_q != N_k and large logits."""
+"""The forward kernels (fa_debug_set_fwd_form: 1 one query tile per CTA, 2 two
+query tiles per CTA taking turns on the tensor pipe (d = 128), 3 one CTA per SM
+taking query tiles from a queue) run the same arithmetic on each row in the same
+order, so O and L must agree bit for bit; forms 2 and 3 are also checked against
+the float64 oracle, over masks, ragged and odd tile counts (a last CTA with one
+query tile), N_q != N_k and large logits."""
 import math
 
 import pytest
@@ -37,8 +38,8 @@ def _fwd(form, Q, K, V, causal, window, counter=None):
     return o.cpu(), lse.cpu()
 
 
-def _inputs(B, H, Nq, Nk, seed, qk_mult=1.0):
-    Q, K, V, _ = si.make_qkvdo(B, H, max(Nq, Nk), 128, seed=seed, qk_mult=qk_mult)
+def _inputs(B, H, Nq, Nk, seed, qk_mult=1.0, d=128):
+    Q, K, V, _ = si.make_qkvdo(B, H, max(Nq, Nk), d, seed=seed, qk_mult=qk_mult)
     return Q[:, :, :Nq].contiguous(), K[:, :, :Nk].contiguous(), V[:, :, :Nk].contiguous()
 
 
@@ -48,28 +49,42 @@ CASES = [(1, 256, 256, False, 0), (1, 256, 256, True, 0), (2, 384, 384, True, 0)
          (1, 640, 2000, True, 256), (2, 128, 128, True, 0)]
 
 
+@pytest.mark.parametrize("form", [2, 3])
 @pytest.mark.parametrize("H,Nq,Nk,causal,window", CASES)
-def test_two_tile_form_equals_one_tile_form(H, Nq, Nk, causal, window):
+def test_other_forms_equal_one_tile_form(form, H, Nq, Nk, causal, window):
     Q, K, V = _inputs(1, H, Nq, Nk, seed=1900 + Nq + Nk + window)
     cnt = torch.zeros(2, dtype=torch.int64, device="cuda")
     o1, l1 = _fwd(1, Q, K, V, causal, window, counter=cnt[0:1])
-    o2, l2 = _fwd(2, Q, K, V, causal, window, counter=cnt[1:2])
+    o2, l2 = _fwd(form, Q, K, V, causal, window, counter=cnt[1:2])
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
     assert cnt[0].item() == cnt[1].item() == H * lib().fa_tile_pairs_ex(Nq, Nk, 128, causal, window, 0)
 
 
+@pytest.mark.parametrize("d", [32, 64])
+@pytest.mark.parametrize("B,H,Nq,Nk,causal,window", [(2, 3, 1000, 1000, True, 0), (1, 5, 300, 700, False, 0),
+                                                      (3, 2, 777, 777, True, 100), (1, 1, 1, 300, True, 0),
+                                                      (4, 40, 256, 256, True, 0)])
+def test_persistent_form_equals_one_tile_form_small_heads(d, B, H, Nq, Nk, causal, window):
+    Q, K, V = _inputs(B, H, Nq, Nk, seed=2100 + Nq + d, d=d)
+    o1, l1 = _fwd(1, Q, K, V, causal, window)
+    o3, l3 = _fwd(3, Q, K, V, causal, window)
+    assert torch.equal(o1, o3) and torch.equal(l1, l3)
+
+
+@pytest.mark.parametrize("form", [2, 3])
 @pytest.mark.parametrize("H,Nq,Nk,causal,window,qk", [(2, 1000, 1000, True, 0, 1.0), (2, 700, 700, False, 0, 4.0),
                                                       (2, 900, 900, True, 200, 4.0), (1, 300, 1000, True, 0, 1.0)])
-def test_two_tile_form_matches_oracle(H, Nq, Nk, causal, window, qk):
+def test_other_forms_match_oracle(form, H, Nq, Nk, causal, window, qk):
     Q, K, V = _inputs(1, H, Nq, Nk, seed=2000 + Nq, qk_mult=qk)
-    o, lse = _fwd(2, Q, K, V, causal, window)
+    o, lse = _fwd(form, Q, K, V, causal, window)
     O, L = oracle.standard_attention_fwd(f64(Q), f64(K), f64(V), causal, window=window)
-    assert_close({"O": f64(o), "L": f64(lse)}, {"O": O, "L": L}, f"two-tile form Nq={Nq} Nk={Nk} w={window}")
+    assert_close({"O": f64(o), "L": f64(lse)}, {"O": O, "L": L}, f"form {form} Nq={Nq} Nk={Nk} w={window}")
 
 
-def test_two_tile_form_long_shape_equals_one_tile_form():
+@pytest.mark.parametrize("form", [2, 3])
+def test_other_forms_long_shape_equal_one_tile_form(form):
     w = si.WORKLOADS["long_1x32x8192x128"]
     Q, K, V, _ = si.make_workload(w)
     o1, l1 = _fwd(1, Q, K, V, True, 0)
-    o2, l2 = _fwd(2, Q, K, V, True, 0)
+    o2, l2 = _fwd(form, Q, K, V, True, 0)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
