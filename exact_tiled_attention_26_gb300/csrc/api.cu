@@ -247,8 +247,25 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int 
 // the fp32 workspace, 2 = two kernels (key tiles for dK, dV; query tiles for dQ).
 static int bwd_split(int d) {
   if (d != 128 && d != 64) return 1;
+  if (g_bwd_split == 3) return d == 128 ? 3 : 1;  // the persistent form exists at d = 128
   if (g_bwd_split != 0) return g_bwd_split;
   return d == 128 ? kDefaultBwdSplitD128 : kDefaultBwdSplitD64;
+}
+
+// Whether the d = 128 one-kernel backward runs persistent (form 3).  Measured on
+// GB300, backward TFLOP/s form 1 -> form 3: 8 x 16 x 2048 causal 682 -> 737, the
+// long shape with a 1024-key window 640 -> 680, 2 x 16 x 4096 causal 866 -> 902,
+// non-causal 1025 -> 1047, 1 x 32 x 8192 causal 1050 -> 1072; at 1 x 32 x 32768
+// causal (256 query tiles per key tile) the two are level.
+static bool bwd_persistent_pays(int Nq, int Nk, bool causal, int window) {
+  const int Tk = (Nk + kBwdBc - 1) / kBwdBc;
+  for (int kt = 0; kt < Tk; ++kt) {  // the widest ranges are at the start (causal) or inside (window)
+    int lo = 0, hi = -1;
+    query_tile_range(kt, bwd_br(128), kBwdBc, Nq, Nk, causal, window, &lo, &hi);
+    if (hi - lo + 1 > 128) return false;
+    if (window == 0) break;  // without a window the first key tile is seen by the most
+  }
+  return true;
 }
 
 size_t fa_bwd_workspace_size_ex(int B, int H, int Nq, int Nk, int d, int causal, int window) {
@@ -269,7 +286,7 @@ fa_status fa_debug_set_fwd_form(int form) {
 }
 
 fa_status fa_debug_set_bwd_split(int split) {
-  if (split < 0 || split > 2) return FA_ERR_INVALID_ARG;
+  if (split < 0 || split > 3) return FA_ERR_INVALID_ARG;
   g_bwd_split = split;
   return FA_OK;
 }
@@ -302,9 +319,11 @@ fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, 
   if (status == nullptr) return FA_ERR_CUDA;
   BwdLaunch a{Q,  K,  V,  dO, L,      D,     static_cast<float*>(workspace), dK,     dV,
               B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
-  if (bwd_split(d) == 2) return launch_bwd_two_kernel(a, dQ);
+  int split = bwd_split(d);
+  if (split == 1 && d == 128 && g_bwd_split == 0 && bwd_persistent_pays(Nq, Nk, causal != 0, window)) split = 3;
+  if (split == 2) return launch_bwd_two_kernel(a, dQ);
   if (cudaMemsetAsync(workspace, 0, need, stream) != cudaSuccess) return FA_ERR_CUDA;
-  st = launch_bwd(a);
+  st = split == 3 ? launch_bwd_d128_persist(a) : launch_bwd(a);
   if (st != FA_OK) return st;
   return launch_dq_convert(static_cast<const float*>(workspace), dQ, static_cast<long long>(B) * H * Nq * d, scale,
                            stream);

@@ -127,6 +127,8 @@ fa_status launch_bwd(const BwdLaunch& a);
 fa_status launch_bwd_d128(const BwdLaunch& a);
 // Two-kernel backward (d = 64 or 128): dK, dV by key tile, then dQ by query tile,
 // written directly to dQ (bf16); needs no workspace.
+// d = 128 one-kernel backward, one CTA per SM taking key tiles from a queue (bwd128p.cu).
+fa_status launch_bwd_d128_persist(const BwdLaunch& a);
 fa_status launch_bwd_two_kernel(const BwdLaunch& a, void* dQ);
 
 fa_status launch_preprocess(const void* O, const void* dO, float* D, long long rows, int d, cudaStream_t s);

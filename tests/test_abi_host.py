@@ -115,11 +115,12 @@ def test_tile_pair_counts_for_the_workloads(fa_lib):
 
 
 def test_backward_split_selection(fa_lib):
-    """Form 2 (two kernels) writes dQ directly and needs no workspace; form 1 needs
-    the fp32 dQ accumulator; d = 32 always uses form 1."""
+    """Form 2 (two kernels) writes dQ directly and needs no workspace; forms 1 and 3
+    (one kernel, the latter persistent) need the fp32 dQ accumulator; d = 32 always
+    uses form 1."""
     fa = fa_lib
     try:
-        assert fa.fa_debug_set_bwd_split(3) == fa.FA_ERR_INVALID_ARG
+        assert fa.fa_debug_set_bwd_split(4) == fa.FA_ERR_INVALID_ARG
         assert fa.fa_debug_set_bwd_split(-1) == fa.FA_ERR_INVALID_ARG
         assert fa.fa_debug_set_bwd_split(2) == fa.FA_OK
         assert fa.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 0
@@ -127,6 +128,9 @@ def test_backward_split_selection(fa_lib):
         assert fa.fa_bwd_workspace_size(2, 16, 4096, 32, 1) == 2 * 16 * 4096 * 32 * 4
         assert fa.fa_debug_set_bwd_split(1) == fa.FA_OK
         assert fa.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 2 * 16 * 4096 * 128 * 4
+        assert fa.fa_debug_set_bwd_split(3) == fa.FA_OK
+        assert fa.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 2 * 16 * 4096 * 128 * 4
+        assert fa.fa_bwd_workspace_size(2, 16, 4096, 64, 1) == 2 * 16 * 4096 * 64 * 4
     finally:
         fa.fa_debug_set_bwd_split(0)
 

@@ -1,9 +1,11 @@
-"""GPU parity of both forms of the d = 64 and d = 128 backward ("CS336 Assignment 2 notes"
-§1.4): form 1 (one kernel over key tiles, dQ reduced in an fp32 workspace) and
-form 2 (a key-tile kernel for dK, dV and a query-tile kernel for dQ), each
-against the float64 oracle, whichever of them is the library's default."""
+"""GPU parity of the forms of the d = 64 and d = 128 backward ("CS336 Assignment 2
+notes" §1.4): form 1 (one kernel over key tiles, dQ reduced in an fp32 workspace),
+form 2 (a key-tile kernel for dK, dV and a query-tile kernel for dQ) and form 3
+(form 1 with one CTA per SM taking key tiles from a queue; d = 128), each against
+the float64 oracle, whichever of them is the library's default."""
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import seeded_inputs as si
@@ -11,7 +13,7 @@ from gpu_util import assert_close, f64, lib, rel_frob, run_gpu
 
 pytestmark = pytest.mark.gpu
 
-SPLITS = [1, 2]
+SPLITS = [1, 2, 3]
 
 
 def _oracle_full(Q, K, V, dO, causal, scale=None):
@@ -89,3 +91,16 @@ def test_small_workload_form2_d64(causal):
     ref = _oracle_full(Q, K, V, dO, causal)
     assert_close(_grads(got), {n: ref[n] for n in ("dQ", "dK", "dV")}, "small form 2")
     assert got["tiles"][1] == 32 * lib().fa_tile_pairs(1024, 64, causal, 1)
+
+
+@pytest.mark.parametrize("B,H,N,causal,window", [(2, 3, 1000, True, 0), (1, 5, 700, False, 0), (3, 2, 777, True, 100),
+                                                 (4, 40, 256, True, 0), (2, 16, 4096, True, 0)])
+def test_persistent_form_equals_form1(B, H, N, causal, window):
+    """Form 3 runs each key tile exactly as form 1 does: dK and dV agree bit for bit;
+    dQ is summed in fp32 reductions whose order varies."""
+    Q, K, V, dO = si.make_qkvdo(B, H, N, 128, seed=2200 + N + window)
+    a = run_gpu(Q, K, V, dO, causal, counter=True, split=1, window=window)
+    b = run_gpu(Q, K, V, dO, causal, counter=True, split=3, window=window)
+    assert torch.equal(a["dK"], b["dK"]) and torch.equal(a["dV"], b["dV"])
+    assert rel_frob(f64(b["dQ"]), f64(a["dQ"])) <= 2e-3
+    assert a["tiles"] == b["tiles"]

@@ -50,7 +50,7 @@ def test_sliding_window(d, N, window):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("split", [1, 2])
+@pytest.mark.parametrize("split", [1, 2, 3])
 @pytest.mark.parametrize("N,window", [(1000, 100), (777, 256), (300, 1)])
 def test_sliding_window_both_backward_forms(d, split, N, window):
     _check(N, N, d, True, window, seed=500 + N + window, split=split)
@@ -66,7 +66,7 @@ def test_unequal_lengths(d, Nq, Nk, causal, window):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("split", [1, 2])
+@pytest.mark.parametrize("split", [1, 2, 3])
 def test_unequal_lengths_both_backward_forms(d, split):
     _check(300, 1000, d, True, 0, seed=700, split=split)
     _check(1000, 300, d, False, 0, seed=701, split=split)

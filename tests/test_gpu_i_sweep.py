@@ -26,8 +26,8 @@ def _case(seed):
     Nk = int(rng.integers(1, 700))
     Nq = int(rng.integers(1, Nk + 1)) if causal else int(rng.integers(1, 700))
     window = int(rng.integers(1, 2 * Nk + 2)) if causal and rng.integers(0, 2) else 0
-    split = int(rng.choice([0, 1, 2])) if d >= 64 else 0
-    form = int(rng.choice([0, 1, 2])) if d == 128 else 0
+    split = int(rng.choice([0, 1, 2, 3])) if d >= 64 else 0
+    form = int(rng.choice([0, 1, 2, 3])) if d == 128 else int(rng.choice([0, 1, 3]))
     host = bool(rng.integers(0, 3) == 0)
     hpc = int(rng.integers(0, B * H + 1))
     return d, B, H, Nq, Nk, causal, window, split, form, host, hpc
