@@ -191,12 +191,14 @@ fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter) {
 
 // Which forward kernel runs (fa_debug_set_fwd_form overrides).  Measured on GB300,
 // forward TFLOP/s: the persistent kernel (form 3) hides most of the fixed cost of a
-// CTA and wins whenever query tiles see few key tiles, e.g. at d = 128 the 1024-key
-// window on 1 x 32 x 8192 763 against 689 (one tile per CTA) and 732 (two tiles per
-// CTA), 8 x 16 x 2048 causal 887 against 804 and 840, 2 x 16 x 4096 causal 1035
-// against 1007, and at d = 64 every shape measured (2 x 16 x 4096 causal 628 against
-// 586); with long key ranges at d = 128 (1 x 32 x 32768 causal, a 2048-query prefill
-// chunk of 32768 keys) the one-tile kernel is 2-3% faster.
+// CTA and wins unless query tiles see very many key tiles, e.g. at d = 128 the
+// 1024-key window on 1 x 32 x 8192 807 against 689 (one tile per CTA) and 732 (two
+// tiles per CTA), 8 x 16 x 2048 causal 946 against 804 and 840, 1 x 32 x 8192
+// causal 1289 against 1238, 1 x 32 x 16384 causal (up to 128 key tiles) 1340-1392
+// against 1304-1368, and at d = 64 every shape measured (2 x 16 x 4096 causal 652
+// against 586); with up to 256 key tiles per query tile (1 x 32 x 32768 causal,
+// 32768 non-causal, a 2048-query prefill chunk of 32768 keys) the one-tile kernel is
+// 1-2% faster.
 static int fwd_form(int d, int Nq, int Nk, bool causal, int window) {
   if (g_fwd_form != 0) return (g_fwd_form == 2 && d != 128) ? 1 : g_fwd_form;
   if (d != 128) return 3;
@@ -204,7 +206,7 @@ static int fwd_form(int d, int Nq, int Nk, bool causal, int window) {
   for (int qt = T - 1; qt >= 0; --qt) {  // the widest ranges are at the end (causal) or inside (window)
     int lo = 0, hi = -1;
     key_tile_range(qt, kFwdBr, kFwdBc, Nq, Nk, causal, window, &lo, &hi);
-    if (hi - lo + 1 > 48) return 1;
+    if (hi - lo + 1 > 128) return 1;
     if (window == 0) break;  // without a window the last query tile sees the most
   }
   return 3;

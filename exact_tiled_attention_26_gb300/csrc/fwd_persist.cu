@@ -17,8 +17,12 @@
 // then loads that unit's Q (two buffers) and K, V tiles (a 2-stage ring whose
 // position runs on across units); warp 1 issues S = Q K_j^T into three 128-column
 // tensor-memory buffers (position running on across units); warp 2 issues
-// O += P_j V_j; warps 4..7 run the softmax and, per unit, the epilogue, which
-// releases O to the next unit's first P V product before storing.
+// O += P_j V_j; warps 4..7 run the softmax and hand each unit's row state (running
+// max and sums) to warps 8..11 through shared memory, then go straight on to the
+// next unit; warps 8..11 wait for the unit's last P V product, take O out of
+// tensor memory, release it to the next unit's first product and store O and L.
+// Registers move with setmaxnreg: 56 (TMA, UMMA issue) + 232 (softmax) + 216
+// (epilogue) = 3 x 168.
 #include <mutex>
 
 #include "fwd_softmax.cuh"
@@ -49,10 +53,15 @@ struct PCfg {
   static constexpr int NSB = 3;
   static constexpr int B_UFULL = 0, B_UEMPTY = 2, B_QFULL = 4, B_QEMPTY = 6, B_KFULL = 8, B_KEMPTY = 10,
                        B_VFULL = 12, B_VEMPTY = 14, B_SFULL = 16, B_PFULL = 19, B_PFREE = 22, B_OFULL = 25,
-                       B_OFREE = 26, B_SDONE = 27, B_PVDONE = 28, NBAR = 29;
-  static constexpr int UEMPTY_COUNT = 1 + 1 + 4;  // S issuer, P V issuer, the 4 softmax warps
+                       B_OFREE = 26, B_SDONE = 27, B_PVDONE = 28,
+                       B_EREADY = 29,  // [unit parity] row state of the unit written by the softmax warps
+                       B_EFREE = 31,   // [unit parity] read by the epilogue warps
+                       NBAR = 33;
+  static constexpr int NTHREADS = 384;
+  static constexpr int UEMPTY_COUNT = 1 + 1 + 4 + 4;  // S issuer, P V issuer, 4 softmax and 4 epilogue warps
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tensor-memory base, abort flag, unit ring
-  static constexpr int SMEM_USED = OFF_MISC + 16;
+  static constexpr int OFF_ROWS = OFF_MISC + 16;       // [2][3][128] floats: m, l, l of the bf16 weights
+  static constexpr int SMEM_USED = OFF_ROWS + 2 * 3 * BM * 4;
   static constexpr int SMEM = (SMEM_USED + 1024 > 120 * 1024) ? SMEM_USED + 1024 : 120 * 1024;
   static constexpr int TM_S0 = 0, TM_O = NSB * 128, TM_COLS = 512;
   static_assert(TM_O + D <= TM_COLS, "tensor memory budget");
@@ -78,7 +87,7 @@ FA_DEV Unit decode_unit(int u, int T, int BH, int hg, int Nq, int Nk, bool causa
 }
 
 template <int D, int MASK>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(PCfg<D>::NTHREADS, 1)
     fwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
                        float* __restrict__ Lout, int BH, int Nq, int Nk, int window, float c_log2, int head_group,
@@ -120,6 +129,10 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(bar(C::B_OFREE), 128);
     mbar_init(bar(C::B_SDONE), 1);
     mbar_init(bar(C::B_PVDONE), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::B_EREADY + i), 128);
+      mbar_init(bar(C::B_EFREE + i), 128);
+    }
     *abort_flag = (*reinterpret_cast<volatile int*>(status) != 0);
     fence_mbar_init();
   }
@@ -137,6 +150,10 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = *tmem_slot;
   const bool skip = *abort_flag != 0;
 
+  float* rows = reinterpret_cast<float*>(smem + C::OFF_ROWS);
+
+  if (warp < 4) {
+  regs_dec<56>();
   if (warp == 0 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- producer
     int kv = 0, jk = -1, jv = -1, kq = -1;  // K/V tiles issued; last K, V, Q load issued
@@ -249,8 +266,11 @@ __global__ void __launch_bounds__(256, 1)
     }
     // every S completed before its P existed, so this marks the end of all UMMAs
     mma_commit(bar(C::B_PVDONE));
-  } else if (warp >= 4 && !skip) {
-    // ---------------------------------------------------------------- softmax + epilogue
+  }
+  } else if (warp < 8) {
+  regs_inc<232>();
+  if (!skip) {
+    // ---------------------------------------------------------------- softmax
     const int wq = warp & 3;
     const int row = wq * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
@@ -284,6 +304,41 @@ __global__ void __launch_bounds__(256, 1)
         mbar_arrive(bar(C::B_PFULL + b));
       }
       if (!ok) break;
+      // the row state of this unit for the epilogue warps (slot k % 2 last held unit
+      // k-2's, which they have read)
+      if (k >= 2 && !(ok = mbar_wait_warp(bar(C::B_EFREE + slot), ((k >> 1) & 1) ^ 1, guard, SITE_PF_SOFTMAX)))
+        break;
+      float* rs = rows + slot * 3 * C::BM;
+      rs[row] = st.m_run;
+      rs[C::BM + row] = st.l_run;
+      rs[2 * C::BM + row] = st.lr_run;
+      mbar_arrive(bar(C::B_EREADY + slot));
+    }
+  }
+  } else {
+  regs_inc<216>();  // from the launch's 168: an increase
+  if (!skip) {
+    // ---------------------------------------------------------------- epilogue
+    const int wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const int slot = k & 1;
+      if (!(ok = mbar_wait_warp(bar(C::B_UFULL + slot), (k >> 1) & 1, guard, SITE_PF_SOFTMAX))) break;
+      const int u = unit_ring[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_UEMPTY + slot));
+      if (u < 0) break;
+      const Unit x = decode_unit(u, T, BH, head_group, Nq, Nk, CAUSAL, w);
+      const int q = x.qt * C::BM + row;
+      if (!(ok = mbar_wait_warp(bar(C::B_EREADY + slot), (k >> 1) & 1, guard, SITE_PF_SOFTMAX))) break;
+      const float* rs = rows + slot * 3 * C::BM;
+      SoftmaxRow st;
+      st.m_run = rs[row];
+      st.l_run = rs[C::BM + row];
+      st.lr_run = rs[2 * C::BM + row];
+      mbar_arrive(bar(C::B_EFREE + slot));
       if (!(ok = mbar_wait_warp(bar(C::B_OFULL), k & 1, guard, SITE_PF_SOFTMAX))) break;
       tc_fence_after();
       uint32_t pk[D / 2];
@@ -295,6 +350,7 @@ __global__ void __launch_bounds__(256, 1)
         softmax_epilogue_store<D>(st, pk, O + r0 * D, Lout + r0);
       }
     }
+  }
   }
 
   tc_fence_before();
@@ -347,7 +403,7 @@ fa_status launch_persist_t(const FwdLaunch& a) {
   const long long units = static_cast<long long>((a.Nq + C::BM - 1) / C::BM) * a.BH;
   const int grid = static_cast<int>(units < nsm ? units : nsm);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  kern<<<grid, 256, C::SMEM, a.stream>>>(mQ, mK, mV, static_cast<__nv_bfloat16*>(a.O), a.L, a.BH, a.Nq, a.Nk,
+  kern<<<grid, C::NTHREADS, C::SMEM, a.stream>>>(mQ, mK, mV, static_cast<__nv_bfloat16*>(a.O), a.L, a.BH, a.Nq, a.Nk,
                                          a.window, c_log2, head_group(a.BH, a.Nq, a.Nk, D), counter, a.status,
                                          a.counter);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;

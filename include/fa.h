@@ -275,7 +275,7 @@ fa_status fa_debug_set_bwd_split(int split);
  *      a static device array (no allocation) and zeroes it on its stream; at
  *      most 1024 such launches may be in flight at once across streams;
  *   0: the library's default, chosen by measurement on GB300: form 3 for d <= 64,
- *      and for d = 128 when no query tile sees more than 48 key tiles; else 1.
+ *      and for d = 128 when no query tile sees more than 128 key tiles; else 1.
  * Process-wide setting; FA_ERR_INVALID_ARG for other values.
  */
 fa_status fa_debug_set_fwd_form(int form);
