@@ -343,7 +343,8 @@ def run_ours(args):
         "frac_of_bf16_peak": round(value / world / sustained, 4),
         "roofline": {
             "bound": "tensor",
-            "kernel": "bwd_d128_kernel (timed as the fa_bwd call: main kernel + workspace clear + dQ convert)",
+            "kernel": ("the d=128 backward main kernel (bwd_d128_kernel, or bwd_d128p_kernel where the library runs "
+                       "it persistent), timed as the fa_bwd call: main kernel + workspace clear + dQ convert"),
             "achieved": round(bwd_tflops, 2), "peak": sustained, "unit": "TFLOP/s",
             "frac": round(bwd_tflops / sustained, 4),
             "traffic": None if args.window else _TRAFFIC.get((w.name, causal)),
