@@ -356,6 +356,9 @@ def run_ours(args):
     }
     if args.window:
         line["config"]["window"] = args.window
+    st_forms, f_form, b_form = fa.fa_selected_forms(w.N, w.N, w.d, causal, args.window)
+    if st_forms == fa.FA_OK:
+        line["config"]["forms"] = {"fwd": f_form, "bwd": b_form}
     if not args.quick and rank == 0:
         # end to end through the C ABI with host buffers
         steps_e2e = max(2, min(args.steps, 5))

@@ -199,7 +199,7 @@ fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter) {
 // against 586); with up to 256 key tiles per query tile (1 x 32 x 32768 causal,
 // 32768 non-causal, a 2048-query prefill chunk of 32768 keys) the one-tile kernel is
 // 1-2% faster.
-static int fwd_form(int d, int Nq, int Nk, bool causal, int window) {
+static int fwd_form_for(int d, int Nq, int Nk, bool causal, int window) {
   if (g_fwd_form != 0) return (g_fwd_form == 2 && d != 128) ? 1 : g_fwd_form;
   if (d != 128) return 3;
   const int T = (Nq + kFwdBr - 1) / kFwdBr;
@@ -225,7 +225,7 @@ fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float*
   int* status = device_status_word();
   if (status == nullptr) return FA_ERR_CUDA;
   FwdLaunch a{Q, K, V, O, L, B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
-  const int form = fwd_form(d, Nq, Nk, causal != 0, window);
+  const int form = fwd_form_for(d, Nq, Nk, causal != 0, window);
   return form == 2 ? launch_fwd_pp(a) : form == 3 ? launch_fwd_persist(a) : launch_fwd(a);
 }
 
@@ -270,6 +270,14 @@ static bool bwd_persistent_pays(int Nq, int Nk, bool causal, int window) {
   return true;
 }
 
+// The backward form that runs: the split (bwd_split), made persistent at d = 128
+// where that pays.
+static int bwd_form_for(int d, int Nq, int Nk, bool causal, int window) {
+  const int split = bwd_split(d);
+  if (split == 1 && d == 128 && g_bwd_split == 0 && bwd_persistent_pays(Nq, Nk, causal, window)) return 3;
+  return split;
+}
+
 size_t fa_bwd_workspace_size_ex(int B, int H, int Nq, int Nk, int d, int causal, int window) {
   bool empty = false;
   if (check_mask_shape(B, H, Nq, Nk, d, causal, window, &empty) != FA_OK) return static_cast<size_t>(-1);
@@ -279,6 +287,16 @@ size_t fa_bwd_workspace_size_ex(int B, int H, int Nq, int Nk, int d, int causal,
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
   return fa_bwd_workspace_size_ex(B, H, N, N, d, causal, 0);
+}
+
+fa_status fa_selected_forms(int Nq, int Nk, int d, int causal, int window, int* fwd_form, int* bwd_form) {
+  bool empty = false;
+  if (!fwd_form || !bwd_form) return FA_ERR_INVALID_ARG;
+  const fa_status st = check_mask_shape(1, 1, Nq, Nk, d, causal, window, &empty);
+  if (st != FA_OK) return st;
+  *fwd_form = fwd_form_for(d, Nq, Nk, causal != 0, window);
+  *bwd_form = bwd_form_for(d, Nq, Nk, causal != 0, window);
+  return FA_OK;
 }
 
 fa_status fa_debug_set_fwd_form(int form) {
@@ -321,8 +339,7 @@ fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, 
   if (status == nullptr) return FA_ERR_CUDA;
   BwdLaunch a{Q,  K,  V,  dO, L,      D,     static_cast<float*>(workspace), dK,     dV,
               B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
-  int split = bwd_split(d);
-  if (split == 1 && d == 128 && g_bwd_split == 0 && bwd_persistent_pays(Nq, Nk, causal != 0, window)) split = 3;
+  const int split = bwd_form_for(d, Nq, Nk, causal != 0, window);
   if (split == 2) return launch_bwd_two_kernel(a, dQ);
   if (cudaMemsetAsync(workspace, 0, need, stream) != cudaSuccess) return FA_ERR_CUDA;
   st = split == 3 ? launch_bwd_d128_persist(a) : launch_bwd(a);

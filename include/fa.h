@@ -281,6 +281,13 @@ fa_status fa_debug_set_bwd_split(int split);
 fa_status fa_debug_set_fwd_form(int form);
 
 /*
+ * Which forms fa_fwd_ex and fa_bwd_ex would run for these sizes and mask under
+ * the current settings (the numbers of fa_debug_set_fwd_form and
+ * fa_debug_set_bwd_split).  Host only; the argument checks of fa_fwd_ex.
+ */
+fa_status fa_selected_forms(int Nq, int Nk, int d, int causal, int window, int* fwd_form, int* bwd_form);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of the
  * current device.  FA_OK if no kernel has given up since the last poll;
  * FA_ERR_TIMEOUT otherwise, with the failing wait site in *detail (may be NULL).

@@ -175,3 +175,33 @@ def test_forward_form_switch(fa_lib):
         assert fa.fa_debug_set_fwd_form(form) == fa.FA_OK
     assert fa.fa_debug_set_fwd_form(4) == fa.FA_ERR_INVALID_ARG
     assert fa.fa_debug_set_fwd_form(-1) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("Nq,Nk,d,causal,window,fwd,bwd", [
+    (32768, 32768, 128, 1, 0, 1, 1),   # 256 key tiles per query tile: the one-tile kernels
+    (32768, 32768, 128, 0, 0, 1, 1),
+    (16384, 16384, 128, 1, 0, 3, 3),   # up to 128: persistent
+    (8192, 8192, 128, 1, 0, 3, 3),
+    (4096, 4096, 128, 0, 0, 3, 3),
+    (8192, 8192, 128, 1, 1024, 3, 3),  # a window: few tiles per row
+    (2048, 32768, 128, 1, 0, 1, 3),    # prefill: long rows, short key-tile loops
+    (1024, 1024, 64, 1, 0, 3, 2),      # d = 64: persistent forward, two-kernel backward
+    (256, 256, 32, 0, 0, 3, 1),        # d = 32: persistent forward, one-kernel backward
+])
+def test_selected_forms(fa_lib, Nq, Nk, d, causal, window, fwd, bwd):
+    assert fa_lib.fa_selected_forms(Nq, Nk, d, causal, window) == (fa_lib.FA_OK, fwd, bwd)
+
+
+def test_selected_forms_follow_overrides(fa_lib):
+    fa = fa_lib
+    try:
+        fa.check(fa.fa_debug_set_fwd_form(1))
+        fa.check(fa.fa_debug_set_bwd_split(2))
+        assert fa.fa_selected_forms(4096, 4096, 128, 1, 0) == (fa.FA_OK, 1, 2)
+        fa.check(fa.fa_debug_set_fwd_form(2))
+        assert fa.fa_selected_forms(4096, 4096, 64, 1, 0)[1] == 1  # two query tiles per CTA exists at d = 128 only
+    finally:
+        fa.fa_debug_set_fwd_form(0)
+        fa.fa_debug_set_bwd_split(0)
+    assert fa.fa_selected_forms(100, 100, 48, 1, 0)[0] == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_selected_forms(100, 100, 64, 0, 8)[0] == fa.FA_ERR_INVALID_ARG
