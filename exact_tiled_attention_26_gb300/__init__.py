@@ -22,7 +22,7 @@ __all__ = [
     "fa_bwd_noalloc", "FA_NOALLOC_MAX_WORKSPACE_BYTES",
     "fa_fwd_bwd_host", "fa_fwd_bwd_host_workspace_size", "fa_fwd_bwd_host_chunk_heads",
     "fa_status_string", "fa_get_tile_config", "fa_tile_pairs", "fa_debug_set_tile_counter", "fa_debug_set_bwd_split",
-    "fa_debug_set_fwd_form", "fa_selected_forms",
+    "fa_debug_set_fwd_form", "fa_selected_forms", "fa_debug_bwd_plan", "fa_debug_set_kernel_events",
     "fa_poll_device_error", "fa_debug_timeout_probe", "fa_selftest_umma", "fa_version",
     "attention_forward", "attention_backward", "attention_fwd_bwd_host", "check",
 ]
@@ -70,6 +70,8 @@ _sig = {
     "fa_debug_set_bwd_split": (_i, [_i]),
     "fa_debug_set_fwd_form": (_i, [_i]),
     "fa_selected_forms": (_i, [_i] * 5 + [ctypes.POINTER(_i)] * 2),
+    "fa_debug_bwd_plan": (_i, [_i] * 7 + [ctypes.POINTER(_i), ctypes.POINTER(_sz)]),
+    "fa_debug_set_kernel_events": (_i, [_i, _vp, _vp]),
     "fa_poll_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
     "fa_debug_timeout_probe": (_i, [_i, _vp]),
     "fa_selftest_umma": (_i, [_i, _vp, _vp, _vp, _i, _i, _vp]),
@@ -172,6 +174,19 @@ def fa_selected_forms(Nq, Nk, d, causal, window):
     f, b = _i(0), _i(0)
     st = lib.fa_selected_forms(Nq, Nk, d, int(bool(causal)), window, ctypes.byref(f), ctypes.byref(b))
     return st, f.value, b.value
+
+
+def fa_debug_bwd_plan(B, H, Nq, Nk, d, causal, window):
+    """(status, backward form, workspace bytes) from one reading of the form setting."""
+    f, n = _i(0), _sz(0)
+    st = lib.fa_debug_bwd_plan(B, H, Nq, Nk, d, int(bool(causal)), window, ctypes.byref(f), ctypes.byref(n))
+    return st, f.value, n.value
+
+
+def fa_debug_set_kernel_events(which, start, stop):
+    """Caller-owned CUDA events (raw cudaEvent_t handles, or None) recorded around the main kernel
+    launch of later forward (which=0) or backward (which=1) calls."""
+    return lib.fa_debug_set_kernel_events(which, start, stop)
 
 
 def fa_poll_device_error(stream):

@@ -1,5 +1,6 @@
 // C ABI of the exact tiled attention library: argument validation, tensor-map
 // encoding and launch of the kernels in fwd.cu, bwd.cu and aux.cu.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -18,9 +19,24 @@ namespace {
 constexpr int kMaxDevices = 64;
 int* g_status_ptr[kMaxDevices] = {nullptr};
 std::mutex g_mu;
-unsigned long long* g_tile_counter = nullptr;
-int g_bwd_split = 0;                    // 0: the defaults below
-int g_fwd_form = 0;                     // 0: the default (fwd_form below)
+// Process-wide debug settings.  Every entry point reads each one exactly once per
+// call (a snapshot) and derives everything from that value, so a concurrent change
+// takes effect on the next call, never halfway through one.
+std::atomic<unsigned long long*> g_tile_counter{nullptr};
+std::atomic<int> g_bwd_split{0};        // 0: the defaults below
+std::atomic<int> g_fwd_form{0};         // 0: the default (fwd_form below)
+// Caller-owned events recorded around the main kernel launch(es) of the forward
+// ([0]) and the backward ([1]); both null when unset.
+struct KernelEvents {
+  cudaEvent_t start = nullptr, stop = nullptr;
+};
+KernelEvents g_kev[2];
+std::mutex g_kev_mu;
+
+KernelEvents kernel_events(int which) {
+  std::lock_guard<std::mutex> lk(g_kev_mu);
+  return g_kev[which];
+}
 constexpr int kDefaultBwdSplitD128 = 1;  // chosen by measurement on GB300
 constexpr int kDefaultBwdSplitD64 = 2;  // two kernels: faster at d = 64 (measured)
 
@@ -185,7 +201,7 @@ long long fa_tile_pairs_ex(int Nq, int Nk, int d, int causal, int window, int pa
 long long fa_tile_pairs(int N, int d, int causal, int pass) { return fa_tile_pairs_ex(N, N, d, causal, 0, pass); }
 
 fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter) {
-  g_tile_counter = dev_counter;
+  g_tile_counter.store(dev_counter);
   return FA_OK;
 }
 
@@ -199,8 +215,8 @@ fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter) {
 // against 586); with up to 256 key tiles per query tile (1 x 32 x 32768 causal,
 // 32768 non-causal, a 2048-query prefill chunk of 32768 keys) the one-tile kernel is
 // 1-2% faster.
-static int fwd_form_for(int d, int Nq, int Nk, bool causal, int window) {
-  if (g_fwd_form != 0) return (g_fwd_form == 2 && d != 128) ? 1 : g_fwd_form;
+static int fwd_form_for(int d, int Nq, int Nk, bool causal, int window, int setting) {
+  if (setting != 0) return (setting == 2 && d != 128) ? 1 : setting;
   if (d != 128) return 3;
   const int T = (Nq + kFwdBr - 1) / kFwdBr;
   for (int qt = T - 1; qt >= 0; --qt) {  // the widest ranges are at the end (causal) or inside (window)
@@ -224,9 +240,13 @@ fa_status fa_fwd_ex(const void* Q, const void* K, const void* V, void* O, float*
     return FA_ERR_INVALID_ARG;
   int* status = device_status_word();
   if (status == nullptr) return FA_ERR_CUDA;
-  FwdLaunch a{Q, K, V, O, L, B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
-  const int form = fwd_form_for(d, Nq, Nk, causal != 0, window);
-  return form == 2 ? launch_fwd_pp(a) : form == 3 ? launch_fwd_persist(a) : launch_fwd(a);
+  FwdLaunch a{Q, K, V, O, L, B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter.load()};
+  const int form = fwd_form_for(d, Nq, Nk, causal != 0, window, g_fwd_form.load());
+  const KernelEvents ev = kernel_events(0);
+  if (ev.start != nullptr && cudaEventRecord(ev.start, stream) != cudaSuccess) return FA_ERR_CUDA;
+  st = form == 2 ? launch_fwd_pp(a) : form == 3 ? launch_fwd_persist(a) : launch_fwd(a);
+  if (st == FA_OK && ev.stop != nullptr && cudaEventRecord(ev.stop, stream) != cudaSuccess) return FA_ERR_CUDA;
+  return st;
 }
 
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* L, int B, int H, int N, int d,
@@ -245,12 +265,13 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int 
   return launch_preprocess(O, dO, D, static_cast<long long>(B) * H * N, d, stream);
 }
 
-// Which backward form runs: 1 = one kernel over key tiles with dQ reduced in
-// the fp32 workspace, 2 = two kernels (key tiles for dK, dV; query tiles for dQ).
-static int bwd_split(int d) {
+// Which backward form runs under the setting `setting` (a snapshot of
+// fa_debug_set_bwd_split): 1 = one kernel over key tiles with dQ reduced in the
+// fp32 workspace, 2 = two kernels (key tiles for dK, dV; query tiles for dQ).
+static int bwd_split(int d, int setting) {
   if (d != 128 && d != 64) return 1;
-  if (g_bwd_split == 3) return d == 128 ? 3 : 1;  // the persistent form exists at d = 128
-  if (g_bwd_split != 0) return g_bwd_split;
+  if (setting == 3) return d == 128 ? 3 : 1;  // the persistent form exists at d = 128
+  if (setting != 0) return setting;
   return d == 128 ? kDefaultBwdSplitD128 : kDefaultBwdSplitD64;
 }
 
@@ -272,17 +293,41 @@ static bool bwd_persistent_pays(int Nq, int Nk, bool causal, int window) {
 
 // The backward form that runs: the split (bwd_split), made persistent at d = 128
 // where that pays.
-static int bwd_form_for(int d, int Nq, int Nk, bool causal, int window) {
-  const int split = bwd_split(d);
-  if (split == 1 && d == 128 && g_bwd_split == 0 && bwd_persistent_pays(Nq, Nk, causal, window)) return 3;
+static int bwd_form_for(int d, int Nq, int Nk, bool causal, int window, int setting) {
+  const int split = bwd_split(d, setting);
+  if (split == 1 && d == 128 && setting == 0 && bwd_persistent_pays(Nq, Nk, causal, window)) return 3;
   return split;
+}
+
+// The backward form and the workspace it needs, both from one snapshot of the
+// setting: a form that reduces dQ in the workspace (1, 3) always comes with the
+// workspace size, the two-kernel form (2) with none.  Shape checked by the caller.
+struct BwdPlan {
+  int form;
+  size_t need;
+};
+static BwdPlan bwd_plan(int B, int H, int Nq, int Nk, int d, bool causal, int window, bool empty, int setting) {
+  BwdPlan p{bwd_form_for(d, Nq, Nk, causal, window, setting), 0};
+  if (!empty && p.form != 2) p.need = static_cast<size_t>(B) * H * Nq * d * sizeof(float);
+  return p;
 }
 
 size_t fa_bwd_workspace_size_ex(int B, int H, int Nq, int Nk, int d, int causal, int window) {
   bool empty = false;
   if (check_mask_shape(B, H, Nq, Nk, d, causal, window, &empty) != FA_OK) return static_cast<size_t>(-1);
-  if (empty || bwd_split(d) == 2) return 0;
-  return static_cast<size_t>(B) * H * Nq * d * sizeof(float);
+  return bwd_plan(B, H, Nq, Nk, d, causal != 0, window, empty, g_bwd_split.load()).need;
+}
+
+fa_status fa_debug_bwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int window, int* form,
+                            size_t* workspace_bytes) {
+  bool empty = false;
+  if (!form || !workspace_bytes) return FA_ERR_INVALID_ARG;
+  const fa_status st = check_mask_shape(B, H, Nq, Nk, d, causal, window, &empty);
+  if (st != FA_OK) return st;
+  const BwdPlan p = bwd_plan(B, H, Nq, Nk, d, causal != 0, window, empty, g_bwd_split.load());
+  *form = p.form;
+  *workspace_bytes = p.need;
+  return FA_OK;
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
@@ -294,20 +339,29 @@ fa_status fa_selected_forms(int Nq, int Nk, int d, int causal, int window, int* 
   if (!fwd_form || !bwd_form) return FA_ERR_INVALID_ARG;
   const fa_status st = check_mask_shape(1, 1, Nq, Nk, d, causal, window, &empty);
   if (st != FA_OK) return st;
-  *fwd_form = fwd_form_for(d, Nq, Nk, causal != 0, window);
-  *bwd_form = bwd_form_for(d, Nq, Nk, causal != 0, window);
+  *fwd_form = fwd_form_for(d, Nq, Nk, causal != 0, window, g_fwd_form.load());
+  *bwd_form = bwd_form_for(d, Nq, Nk, causal != 0, window, g_bwd_split.load());
   return FA_OK;
 }
 
 fa_status fa_debug_set_fwd_form(int form) {
   if (form < 0 || form > 3) return FA_ERR_INVALID_ARG;
-  g_fwd_form = form;
+  g_fwd_form.store(form);
   return FA_OK;
 }
 
 fa_status fa_debug_set_bwd_split(int split) {
   if (split < 0 || split > 3) return FA_ERR_INVALID_ARG;
-  g_bwd_split = split;
+  g_bwd_split.store(split);
+  return FA_OK;
+}
+
+fa_status fa_debug_set_kernel_events(int which, void* start, void* stop) {
+  if (which != 0 && which != 1) return FA_ERR_INVALID_ARG;
+  if ((start == nullptr) != (stop == nullptr)) return FA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_kev_mu);
+  g_kev[which].start = static_cast<cudaEvent_t>(start);
+  g_kev[which].stop = static_cast<cudaEvent_t>(stop);
   return FA_OK;
 }
 
@@ -332,18 +386,27 @@ fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, 
   if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(dO, 16) || !aligned(dQ, 16) ||
       !aligned(dK, 16) || !aligned(dV, 16) || !aligned(L, 4) || !aligned(D, 4))
     return FA_ERR_INVALID_ARG;
-  const size_t need = fa_bwd_workspace_size_ex(B, H, Nq, Nk, d, causal, window);
+  // one snapshot of the setting gives both the form and the workspace it needs
+  const BwdPlan plan = bwd_plan(B, H, Nq, Nk, d, causal != 0, window, false, g_bwd_split.load());
+  const size_t need = plan.need;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
     return FA_ERR_WORKSPACE;
   int* status = device_status_word();
   if (status == nullptr) return FA_ERR_CUDA;
   BwdLaunch a{Q,  K,  V,  dO, L,      D,     static_cast<float*>(workspace), dK,     dV,
-              B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter};
-  const int split = bwd_form_for(d, Nq, Nk, causal != 0, window);
-  if (split == 2) return launch_bwd_two_kernel(a, dQ);
+              B * H, Nq, Nk, d, causal ? 1 : 0, window, scale, stream, status, g_tile_counter.load()};
+  const KernelEvents ev = kernel_events(1);
+  if (plan.form == 2) {
+    if (ev.start != nullptr && cudaEventRecord(ev.start, stream) != cudaSuccess) return FA_ERR_CUDA;
+    st = launch_bwd_two_kernel(a, dQ);
+    if (st == FA_OK && ev.stop != nullptr && cudaEventRecord(ev.stop, stream) != cudaSuccess) return FA_ERR_CUDA;
+    return st;
+  }
   if (cudaMemsetAsync(workspace, 0, need, stream) != cudaSuccess) return FA_ERR_CUDA;
-  st = split == 3 ? launch_bwd_d128_persist(a) : launch_bwd(a);
+  if (ev.start != nullptr && cudaEventRecord(ev.start, stream) != cudaSuccess) return FA_ERR_CUDA;
+  st = plan.form == 3 ? launch_bwd_d128_persist(a) : launch_bwd(a);
   if (st != FA_OK) return st;
+  if (ev.stop != nullptr && cudaEventRecord(ev.stop, stream) != cudaSuccess) return FA_ERR_CUDA;
   return launch_dq_convert(static_cast<const float*>(workspace), dQ, static_cast<long long>(B) * H * Nq * d, scale,
                            stream);
 }

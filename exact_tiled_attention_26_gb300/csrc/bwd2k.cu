@@ -1,7 +1,7 @@
-// Backward pass, head size 128: the two-kernel form of "CS336 Assignment 2
-// notes" §1.4 (kernel 1 iterates key/value tiles in its outer loop and forms
-// dK, dV; kernel 2 iterates query tiles and forms dQ; S and P are computed in
-// both).  No atomics and no workspace: each output is written once.
+// Backward pass, head sizes 64 and 128 (templated on d; the default form at d = 64,
+// selectable at d = 128): the two-kernel form of "CS336 Assignment 2 notes" §1.4 (kernel 1
+// iterates key/value tiles in its outer loop and forms dK, dV; kernel 2 iterates query tiles
+// and forms dQ; S and P are computed in both).  No atomics and no workspace: each output is written once.
 //
 // bwd_kv_kernel: one CTA per 128 keys (keys on the 128 tensor-memory lanes),
 //   S^T = K Q_i^T, dP^T = V dO_i^T (UMMA), P^T, dS^T (16 element-wise warps, 32

@@ -54,16 +54,15 @@ fa_status scratch_on_current_device(void** out) {
 extern "C" fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                                     const float* L, const float* D, void* dQ, void* dK, void* dV, int B, int H,
                                     int N, int d, int causal, float scale, fa_stream_t stream) {
-  const size_t need = fa_bwd_workspace_size(B, H, N, d, causal);
-  if (need == static_cast<size_t>(-1)) return FA_ERR_INVALID_ARG;
-  if (need > fa::kNoallocScratchBytes) return FA_ERR_WORKSPACE;  // problem too large for the fixed array
+  // argument errors first, without touching the device
+  if (fa_bwd_workspace_size(B, H, N, d, causal) == static_cast<size_t>(-1)) return FA_ERR_INVALID_ARG;
   void* scratch = nullptr;
-  if (need > 0) {
-    const fa_status st = fa::scratch_on_current_device(&scratch);
-    if (st != FA_OK) return st;
-  }
-  // fa_bwd validates every argument, zeroes the accumulator on `stream`, then runs
-  // the backward kernels with it.
+  const fa_status st = fa::scratch_on_current_device(&scratch);
+  if (st != FA_OK) return st;
+  // fa_bwd picks the backward form and the accumulator it needs from one reading
+  // of the form setting, rejects a problem whose accumulator is larger than the
+  // array (FA_ERR_WORKSPACE), zeroes the part it uses on `stream`, then runs the
+  // backward kernels with it.
   return fa_bwd(Q, K, V, O, dO, L, D, dQ, dK, dV, B, H, N, d, causal, scale, scratch, fa::kNoallocScratchBytes,
                 stream);
 }

@@ -93,6 +93,7 @@ struct Pipe {
   // per slot: Q, K, V in; dO in; forward done (O, L ready); backward done; every output out
   cudaEvent_t start = nullptr, end = nullptr, in_qkv[kSlots] = {}, in[kSlots] = {}, fwd[kSlots] = {}, done[kSlots] = {},
               out[kSlots] = {};
+  cudaEvent_t drain[1 + kComputeStreams] = {};  // the tails of h2d and the compute streams, on an error
 };
 Pipe g_pipe[kMaxDevices];
 std::mutex g_pipe_mu;  // held for a whole enqueue: the slot events are shared
@@ -104,6 +105,7 @@ bool make_pipe(Pipe* p) {
   auto event = [](cudaEvent_t* e) { return *e != nullptr || cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess; };
   bool ok = stream(&p->h2d) && stream(&p->d2h) && event(&p->start) && event(&p->end);
   for (int i = 0; ok && i < kComputeStreams; ++i) ok = stream(&p->comp[i]);
+  for (int i = 0; ok && i < 1 + kComputeStreams; ++i) ok = event(&p->drain[i]);
   for (int i = 0; ok && i < kSlots; ++i)
     ok = event(&p->in_qkv[i]) && event(&p->in[i]) && event(&p->fwd[i]) && event(&p->done[i]) && event(&p->out[i]);
   p->ready = ok;
@@ -112,6 +114,18 @@ bool make_pipe(Pipe* p) {
 
 bool copy(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, cudaStream_t s) {
   return bytes == 0 || cudaMemcpyAsync(dst, src, bytes, kind, s) == cudaSuccess;
+}
+
+// After a failure midway through an enqueue: copies from or to the caller's host
+// arrays may already be queued on the internal streams.  Order the caller's stream
+// after all of them (best effort: a call that fails here too is skipped), so that
+// synchronising `caller` still means the library no longer touches those arrays.
+void drain_into(Pipe& p, cudaStream_t caller) {
+  cudaStream_t tails[1 + kComputeStreams] = {p.h2d};
+  for (int i = 0; i < kComputeStreams; ++i) tails[1 + i] = p.comp[i];
+  for (int i = 0; i < 1 + kComputeStreams; ++i)
+    if (cudaEventRecord(p.drain[i], tails[i]) == cudaSuccess) cudaStreamWaitEvent(p.d2h, p.drain[i], 0);
+  if (cudaEventRecord(p.end, p.d2h) == cudaSuccess) cudaStreamWaitEvent(caller, p.end, 0);
 }
 
 }  // namespace
@@ -175,6 +189,12 @@ fa_status fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const voi
   for (int i = 0; ok && i < p.streams; ++i) ok = cudaStreamWaitEvent(pp.comp[i], pp.start, 0) == cudaSuccess;
   if (!ok) return FA_ERR_CUDA;
 
+  // from here on part of the step may be enqueued: an error leaves the caller's
+  // stream ordered after whatever was
+  auto fail = [&](fa_status e) {
+    drain_into(pp, stream);
+    return e;
+  };
   for (int c = 0; c < p.chunks; ++c) {
     const int h0 = c * p.hc, hn = (BH - h0) < p.hc ? (BH - h0) : p.hc;
     const int slot = c % p.slots;
@@ -191,25 +211,25 @@ fa_status fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const voi
          cudaEventRecord(pp.in_qkv[slot], pp.h2d) == cudaSuccess &&
          copy(sb + p.slot.dO, hdO + off_q, bq, cudaMemcpyHostToDevice, pp.h2d) &&
          cudaEventRecord(pp.in[slot], pp.h2d) == cudaSuccess;
-    if (!ok) return FA_ERR_CUDA;
+    if (!ok) return fail(FA_ERR_CUDA);
     // compute: the forward after Q, K, V arrived and the slot's previous outputs
     // left; the backward after dO arrived
     if (cudaStreamWaitEvent(cs, pp.in_qkv[slot], 0) != cudaSuccess ||
         (c >= p.slots && cudaStreamWaitEvent(cs, pp.out[slot], 0) != cudaSuccess))
-      return FA_ERR_CUDA;
+      return fail(FA_ERR_CUDA);
     st = fa_fwd_ex(sb + p.slot.q, sb + p.slot.k, sb + p.slot.v, sb + p.slot.o, reinterpret_cast<float*>(sb + p.slot.L),
                    1, hn, Nq, Nk, d, causal, window, scale, cs);
-    if (st != FA_OK) return st;
+    if (st != FA_OK) return fail(st);
     if (cudaEventRecord(pp.fwd[slot], cs) != cudaSuccess || cudaStreamWaitEvent(cs, pp.in[slot], 0) != cudaSuccess)
-      return FA_ERR_CUDA;
+      return fail(FA_ERR_CUDA);
     st = fa_bwd_preprocess(sb + p.slot.o, sb + p.slot.dO, reinterpret_cast<float*>(sb + p.slot.D), 1, hn, Nq, d, cs);
-    if (st != FA_OK) return st;
+    if (st != FA_OK) return fail(st);
     st = fa_bwd_ex(sb + p.slot.q, sb + p.slot.k, sb + p.slot.v, sb + p.slot.o, sb + p.slot.dO,
                    reinterpret_cast<const float*>(sb + p.slot.L), reinterpret_cast<const float*>(sb + p.slot.D),
                    sb + p.slot.dQ, sb + p.slot.dK, sb + p.slot.dV, 1, hn, Nq, Nk, d, causal, window, scale,
                    acc + p.acc_bytes * (c % p.streams), p.acc_bytes, cs);
-    if (st != FA_OK) return st;
-    if (cudaEventRecord(pp.done[slot], cs) != cudaSuccess) return FA_ERR_CUDA;
+    if (st != FA_OK) return fail(st);
+    if (cudaEventRecord(pp.done[slot], cs) != cudaSuccess) return fail(FA_ERR_CUDA);
     // out: O and L once the forward is done, the gradients once the backward is
     ok = cudaStreamWaitEvent(pp.d2h, pp.fwd[slot], 0) == cudaSuccess &&
          copy(hO + off_q, sb + p.slot.o, bq, cudaMemcpyDeviceToHost, pp.d2h) &&
@@ -219,7 +239,7 @@ fa_status fa_fwd_bwd_host(const void* Q, const void* K, const void* V, const voi
          copy(hdK + off_k, sb + p.slot.dK, bk, cudaMemcpyDeviceToHost, pp.d2h) &&
          copy(hdV + off_k, sb + p.slot.dV, bk, cudaMemcpyDeviceToHost, pp.d2h) &&
          cudaEventRecord(pp.out[slot], pp.d2h) == cudaSuccess;
-    if (!ok) return FA_ERR_CUDA;
+    if (!ok) return fail(FA_ERR_CUDA);
   }
   // every chunk's copy out follows its compute, which follows its copy in: the
   // copy-out stream's last event covers the whole step

@@ -32,6 +32,15 @@
  *     limit, and on expiry the kernel records an error in a device status word
  *     and exits; fa_poll_device_error() reads it.
  *   - No N x N buffer is ever allocated or written.
+ *   - The library keeps a few device addresses per device for the life of the
+ *     process (the status word, the work counters of the persistent kernels,
+ *     the array of fa_bwd_noalloc), looked up on first use.  Do not use it
+ *     across cudaDeviceReset() or any other teardown of a device's primary
+ *     context: those addresses would be stale.
+ *   - The debug settings below (fa_debug_*) are process-wide.  Each entry point
+ *     reads each setting once per call and takes every decision of that call
+ *     from that one reading, so a setting changed from another thread applies
+ *     from the next call on.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -199,8 +208,11 @@ fa_status fa_bwd_noalloc(const void* Q, const void* K, const void* V, const void
  *   enqueued on `stream` later is ordered after the last copy back.  The call
  *   returns once all of it is enqueued; the host outputs are valid, and the host
  *   inputs may change again, after `stream` is synchronised.
- * Argument errors return before anything is enqueued; a CUDA failure midway
- * returns FA_ERR_CUDA with part of the step enqueued.
+ * Argument errors return before anything is enqueued.  A failure midway (a CUDA
+ * call, or an error from one chunk's fa_fwd_ex / fa_bwd_ex) returns that status
+ * with part of the step enqueued; `stream` is still ordered after every copy
+ * that was enqueued, so once `stream` is synchronised the library no longer
+ * reads or writes the host arrays.
  * fa_fwd_bwd_host_chunk_heads and fa_fwd_bwd_host_workspace_size are host only
  * (no GPU needed) and return -1 (as size_t for the second) on bad arguments.
  */
@@ -279,6 +291,28 @@ fa_status fa_debug_set_bwd_split(int split);
  * Process-wide setting; FA_ERR_INVALID_ARG for other values.
  */
 fa_status fa_debug_set_fwd_form(int form);
+
+/*
+ * Which backward form fa_bwd_ex would run for these sizes and mask, and the
+ * workspace it would need, both taken from one reading of the
+ * fa_debug_set_bwd_split setting, exactly as fa_bwd_ex takes them: a form that
+ * reduces dQ in the workspace (1, 3) always comes with B*H*Nq*d*4 bytes, the
+ * two-kernel form (2) with 0.  Host only; the argument checks of fa_bwd_ex.
+ */
+fa_status fa_debug_bwd_plan(int B, int H, int Nq, int Nk, int d, int causal, int window, int* form,
+                            size_t* workspace_bytes);
+
+/*
+ * Debug: times the main kernels from the caller's side.  `start` and `stop` are
+ * CUDA events (cudaEvent_t, created and owned by the caller); later calls of
+ * fa_fwd_ex (which = 0) or fa_bwd_ex (which = 1) record `start` on their
+ * stream just before launching their main kernel (the forward kernel; the
+ * backward main kernel, or both kernels of the two-kernel form) and `stop` just
+ * after it, so cudaEventElapsedTime(start, stop) is that launch's device time
+ * (the backward's workspace clear and dQ conversion are outside it).  Both NULL
+ * switch it off; exactly one NULL is FA_ERR_INVALID_ARG.  Process-wide setting.
+ */
+fa_status fa_debug_set_kernel_events(int which, void* start, void* stop);
 
 /*
  * Which forms fa_fwd_ex and fa_bwd_ex would run for these sizes and mask under

@@ -14,8 +14,9 @@ bound on O therefore applies to the error beyond that quantum:
 the relative norm.
 
 With FA_PARITY_LOG set to a file name, every comparison appends its measured
-errors to that file as one JSON line (O: max-abs, max-abs beyond half a bf16
-ulp, rel-Frobenius; L: max-abs; gradients: rel-Frobenius).
+errors to that file as one JSON line: O_max_abs (the raw figure), O_beyond_half_ulp,
+O_rel; L_max_abs; D_max_abs and D_rel when D is compared; dQ_rel, dK_rel, dV_rel
+(or dX_rms where the exact gradient is zero).
 """
 from __future__ import annotations
 
@@ -29,6 +30,19 @@ import torch
 import seeded_inputs as si
 
 TOL_O_ABS, TOL_O_REL, TOL_L_ABS, TOL_G_REL = 1e-2, 5e-3, 2e-3, 1e-2
+TOL_D_REL = 1e-2  # D end to end (no bound is given for it; it follows from O's)
+TOL_D_ELEM = 1e-3  # the preprocess step alone: |D - rowsum(dO * O)| <= 1e-3 * max(1, |D|)
+
+
+def check_D_elementwise(D_gpu, O_gpu, dO):
+    """The preprocess step against its definition on the GPU's own bf16 O: D_i =
+    sum_k dO_ik O_ik in float64, element by element.  Returns the largest error
+    relative to max(1, |D|)."""
+    ref = (f64(dO) * f64(O_gpu)).sum(axis=-1)
+    err = np.abs(f64(D_gpu) - ref) / np.maximum(1.0, np.abs(ref))
+    worst = float(err.max()) if err.size else 0.0
+    assert worst <= TOL_D_ELEM, f"D element-wise {worst:.3e}"
+    return worst
 
 
 def rel_frob(got, ref):
@@ -107,25 +121,30 @@ def assert_close(got: dict, ref: dict, label=""):
     errs = {}
     if "O" in ref:
         ea, ex, er = float(np.abs(got["O"] - ref["O"]).max()), o_excess(got["O"], ref["O"]), rel_frob(got["O"], ref["O"])
-        errs["O"] = (ea, ex, er)
+        errs.update(O_max_abs=ea, O_beyond_half_ulp=ex, O_rel=er)
         if not (ex <= TOL_O_ABS and er <= TOL_O_REL):
             i = np.unravel_index(np.argmax(np.abs(got["O"] - ref["O"])), ref["O"].shape)
             msgs.append(f"O max-abs {ea:.3e} (beyond output rounding {ex:.3e}, at ref {ref['O'][i]:.4f}) rel {er:.3e}")
     if "L" in ref:
         ea = float(np.abs(got["L"] - ref["L"]).max())
-        errs["L"] = ea
+        errs["L_max_abs"] = ea
         if not ea <= TOL_L_ABS:
             msgs.append(f"L max-abs {ea:.3e}")
+    if "D" in ref:  # end to end: D from the GPU's own O, against the oracle's D
+        ea, er = float(np.abs(got["D"] - ref["D"]).max()), rel_frob(got["D"], ref["D"])
+        errs.update(D_max_abs=ea, D_rel=er)
+        if not er <= TOL_D_REL:
+            msgs.append(f"D rel {er:.3e}")
     for n in ("dQ", "dK", "dV"):
         if n in ref:
             if np.linalg.norm(ref[n]) <= 1e-9:
                 rms = float(np.sqrt(np.mean(got[n] ** 2)))
-                errs[n] = rms
+                errs[f"{n}_rms"] = rms
                 if not rms <= 1e-4:
                     msgs.append(f"{n} (exactly zero) rms {rms:.3e}")
                 continue
             er = rel_frob(got[n], ref[n])
-            errs[n] = er
+            errs[f"{n}_rel"] = er
             if not er <= TOL_G_REL:
                 msgs.append(f"{n} rel {er:.3e}")
     log = os.environ.get("FA_PARITY_LOG")

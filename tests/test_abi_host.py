@@ -205,3 +205,49 @@ def test_selected_forms_follow_overrides(fa_lib):
         fa.fa_debug_set_bwd_split(0)
     assert fa.fa_selected_forms(100, 100, 48, 1, 0)[0] == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_selected_forms(100, 100, 64, 0, 8)[0] == fa.FA_ERR_INVALID_ARG
+
+
+def test_bwd_plan_is_one_reading_under_a_flipping_setting(fa_lib):
+    """The backward's form and its workspace size come from one reading of the form
+    setting: while another thread flips fa_debug_set_bwd_split through every value,
+    a form that reduces dQ in the workspace (1, 3) never comes with a zero-byte
+    workspace and the two-kernel form (2) never with a non-zero one."""
+    import threading
+
+    fa = fa_lib
+    B, H, N, d = 2, 3, 1000, 128
+    full = B * H * N * d * 4
+    stop = threading.Event()
+
+    def flip():
+        i = 0
+        while not stop.is_set():
+            fa.fa_debug_set_bwd_split(i % 4)
+            i += 1
+
+    t = threading.Thread(target=flip)
+    t.start()
+    seen = set()
+    try:
+        for _ in range(20000):
+            st, form, need = fa.fa_debug_bwd_plan(B, H, N, N, d, True, 0)
+            assert st == fa.FA_OK
+            assert form in (1, 2, 3)
+            assert need == (0 if form == 2 else full), (form, need)
+            seen.add(form)
+    finally:
+        stop.set()
+        t.join()
+        fa.fa_debug_set_bwd_split(0)
+    assert seen == {1, 2, 3}  # the flips were seen mid-loop
+    assert fa.fa_debug_bwd_plan(B, H, N, N, 48, True, 0)[0] == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_debug_bwd_plan(B, H, 0, N, d, True, 0)[1:] == (3, 0)  # no query rows: nothing to reduce
+
+
+def test_kernel_events_arguments(fa_lib):
+    fa = fa_lib
+    assert fa.fa_debug_set_kernel_events(2, None, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_set_kernel_events(0, 1, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_set_kernel_events(1, None, 1) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_debug_set_kernel_events(0, None, None) == fa.FA_OK
+    assert fa.fa_debug_set_kernel_events(1, None, None) == fa.FA_OK

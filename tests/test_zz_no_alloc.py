@@ -11,8 +11,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import seeded_inputs as si
-from gpu_util import TOL_G_REL, f64, lib, rel_frob, stream
+from gpu_util import TOL_G_REL, assert_close, f64, lib, rel_frob, stream
 
 pytestmark = pytest.mark.gpu
 
@@ -28,14 +29,29 @@ def _forward_and_D(fa, q, k, v, do, causal):
     return o, lse, D
 
 
-@pytest.mark.parametrize("B,H,N,d,causal", [(1, 4, 1000, 128, True), (2, 3, 777, 64, False), (1, 1, 256, 32, True)])
-def test_noalloc_matches_fa_bwd_twice(B, H, N, d, causal):
+# split: the backward form (fa_debug_set_bwd_split; 0 = the library's choice).  The
+# d = 64 case forces the one-kernel form, which accumulates dQ in the array (the
+# library's d = 64 default needs none), so every case exercises the array.
+@pytest.mark.parametrize("B,H,N,d,causal,split", [(1, 4, 1000, 128, True, 0), (2, 3, 777, 64, False, 1),
+                                                  (1, 1, 256, 32, True, 0)])
+def test_noalloc_matches_fa_bwd_twice(B, H, N, d, causal, split):
     """Two calls in a row of the no-allocation entry point give the same dQ, dK,
     dV as fa_bwd with a caller workspace (within the gradient tolerance of the
-    other tests; dQ sums in a different order each call, so not bit for bit).
-    The second call also shows the shared array is cleared between calls."""
+    other tests; dQ sums in a different order each call, so not bit for bit), and
+    both match the float64 oracle.  The second call also shows the shared array is
+    cleared between calls."""
     fa = lib()
+    fa.check(fa.fa_debug_set_bwd_split(split))
+    try:
+        _noalloc_twice(fa, B, H, N, d, causal)
+    finally:
+        fa.fa_debug_set_bwd_split(0)
+
+
+def _noalloc_twice(fa, B, H, N, d, causal):
     Q, K, V, dO = si.make_qkvdo(B, H, N, d, seed=4242 + N)
+    q64, k64, v64, do64 = (f64(t) for t in (Q, K, V, dO))
+    dQ, dK, dV, _ = oracle.standard_attention_bwd(q64, k64, v64, do64, causal)
     q, k, v, do = (t.cuda() for t in (Q, K, V, dO))
     o, lse, D = _forward_and_D(fa, q, k, v, do, causal)
     ref = [torch.empty_like(q) for _ in range(3)]
@@ -55,6 +71,8 @@ def test_noalloc_matches_fa_bwd_twice(B, H, N, d, causal):
             err = rel_frob(f64(g.cpu()), f64(r.cpu()))
             assert err <= TOL_G_REL, f"call {call}: {name} rel {err:.3e}"
         assert torch.equal(got[1], ref[1]) and torch.equal(got[2], ref[2])  # dK, dV: same order of sums
+        assert_close({n: f64(g.cpu()) for n, g in zip(("dQ", "dK", "dV"), got)}, {"dQ": dQ, "dK": dK, "dV": dV},
+                     f"fa_bwd_noalloc call {call} vs oracle")
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
