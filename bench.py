@@ -322,6 +322,7 @@ def run_ours(args):
     w = si.WORKLOADS[args.workload]
     causal = True if len(w.causal) == 1 and w.causal[0] else (args.causal if args.causal is not None else w.causal[-1])
     fa.check(fa.fa_debug_set_bwd_split(args.bwd_split), "fa_debug_set_bwd_split")
+    fa.check(fa.fa_debug_set_fwd_form(args.fwd_form), "fa_debug_set_fwd_form")
     r = Runner(fa, torch, w, causal, dev, window=args.window)
     flops_f, flops_b = w.fwd_flops(causal), w.bwd_flops(causal)
     if args.window:  # FLOPs on the visible entries only
@@ -518,6 +519,9 @@ def main():
     ap.add_argument("--bwd-split", type=int, default=0, choices=[0, 1, 2, 3],
                     help="backward form for d=128: 1 one kernel + dQ reduction, 2 two kernels, 3 form 1 persistent, "
                          "0 library default")
+    ap.add_argument("--fwd-form", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="forward kernel: 1 one query tile per CTA, 2 two per CTA (d=128), 3 persistent, "
+                         "0 library default")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window over the workload's causal mask (with --quick: profiler runs of the "
                          "windowed kernels)")
@@ -526,6 +530,8 @@ def main():
         ap.error("at least 3 warm-up steps")
     if args.window and (not args.quick or args.impl != "ours"):
         ap.error("--window is for --quick runs of this library")
+    if (args.fwd_form or args.bwd_split) and not args.quick:
+        ap.error("--fwd-form and --bwd-split are for --quick runs (the full run times the library's own choice)")
     if args.impl == "reference":
         run_reference(args)
     else:
