@@ -16,6 +16,8 @@
 // Both kernels split UMMA issue over two threads, as the other kernels do.
 #include <type_traits>
 
+#include <mutex>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -585,6 +587,32 @@ __global__ void __launch_bounds__(QC<D>::NTHREADS, 1)
   }
 }
 
+// Side streams for the query-tile kernel, created on first use per device and kept
+// for the process (round robin over a few, so calls on different caller streams
+// rarely share one); each with its own fork and join events.
+struct SideStream {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kSideStreams = 4, kMaxSideDevices = 64;
+SideStream g_side[kMaxSideDevices][kSideStreams];
+int g_side_next[kMaxSideDevices] = {0};
+std::mutex g_side_mu;  // held for a whole fork/join enqueue: the events are shared
+
+fa_status side_stream(SideStream** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return FA_ERR_CUDA;
+  SideStream& ss = g_side[dev][g_side_next[dev]];
+  g_side_next[dev] = (g_side_next[dev] + 1) % kSideStreams;
+  if (ss.s == nullptr && cudaStreamCreateWithFlags(&ss.s, cudaStreamNonBlocking) != cudaSuccess) return FA_ERR_CUDA;
+  if (ss.fork == nullptr && cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (ss.join == nullptr && cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming) != cudaSuccess)
+    return FA_ERR_CUDA;
+  *out = &ss;
+  return FA_OK;
+}
+
 template <int D, bool CAUSAL>
 fa_status launch_t(const BwdLaunch& a, void* dQ) {
   CUtensorMap mQ, mK, mV, mdO;
@@ -594,20 +622,40 @@ fa_status launch_t(const BwdLaunch& a, void* dQ) {
   static_assert(KVC<D>::SMEM <= SMEM_MAX && QC<D>::SMEM <= SMEM_MAX, "shared memory budget");
   auto kkv = bwd_kv_kernel<D, CAUSAL>;
   auto kq = bwd_q_kernel<D, CAUSAL>;
-  if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, KVC<D>::SMEM) != cudaSuccess ||
-      cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, QC<D>::SMEM) != cudaSuccess)
+  // Each CTA takes all 512 tensor-memory columns, so no two CTAs may share an SM
+  // (a second allocation would wait for the first CTA to exit).  Asking for more
+  // than half of the SM's shared memory guarantees it whatever the register counts.
+  constexpr int kExclusive = 120 * 1024;
+  const int smem_kv = KVC<D>::SMEM > kExclusive ? KVC<D>::SMEM : kExclusive;
+  const int smem_q = QC<D>::SMEM > kExclusive ? QC<D>::SMEM : kExclusive;
+  if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_kv) != cudaSuccess ||
+      cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q) != cudaSuccess)
     return FA_ERR_CUDA;
   const int Tq = (a.Nq + 127) / 128, Tk = (a.Nk + 127) / 128;
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  kkv<<<dim3(Tk, a.BH), KVC<D>::NTHREADS, KVC<D>::SMEM, a.stream>>>(
+  // The two kernels are independent (both read Q, K, V, dO, L, D; they write different
+  // outputs), so the query-tile kernel runs on a side stream forked from the caller's:
+  // its CTAs take the SMs that the key-tile kernel's last, partial wave leaves idle
+  // (a CTA of either kernel fills an SM's registers, so they never share one).
+  std::lock_guard<std::mutex> lk(g_side_mu);
+  SideStream* ss = nullptr;
+  const fa_status st = side_stream(&ss);
+  if (st != FA_OK) return st;
+  if (cudaEventRecord(ss->fork, a.stream) != cudaSuccess || cudaStreamWaitEvent(ss->s, ss->fork, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  kkv<<<dim3(Tk, a.BH), KVC<D>::NTHREADS, smem_kv, a.stream>>>(
       mQ, mK, mV, mdO, a.L, a.D, static_cast<__nv_bfloat16*>(a.dK), static_cast<__nv_bfloat16*>(a.dV), a.Nq, a.Nk,
       a.window, c_log2, a.scale, a.status, a.counter, head_group(a.BH, a.Nq, a.Nk, D));
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  kq<<<dim3(Tq, a.BH), QC<D>::NTHREADS, QC<D>::SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D,
-                                                           static_cast<__nv_bfloat16*>(dQ), a.Nq, a.Nk, a.window,
-                                                           c_log2, a.scale, a.status,
-                                                           head_group(a.BH, a.Nq, a.Nk, D));
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  kq<<<dim3(Tq, a.BH), QC<D>::NTHREADS, smem_q, ss->s>>>(mQ, mK, mV, mdO, a.L, a.D,
+                                                        static_cast<__nv_bfloat16*>(dQ), a.Nq, a.Nk, a.window,
+                                                        c_log2, a.scale, a.status,
+                                                        head_group(a.BH, a.Nq, a.Nk, D));
+  // the caller's stream continues only once both kernels are done
+  if (cudaGetLastError() != cudaSuccess || cudaEventRecord(ss->join, ss->s) != cudaSuccess ||
+      cudaStreamWaitEvent(a.stream, ss->join, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 }  // namespace
