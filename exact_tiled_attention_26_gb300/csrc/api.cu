@@ -275,27 +275,16 @@ static int bwd_split(int d, int setting) {
   return d == 128 ? kDefaultBwdSplitD128 : kDefaultBwdSplitD64;
 }
 
-// Whether the d = 128 one-kernel backward runs persistent (form 3).  Measured on
-// GB300, backward TFLOP/s form 1 -> form 3: 8 x 16 x 2048 causal 682 -> 737, the
-// long shape with a 1024-key window 640 -> 680, 2 x 16 x 4096 causal 866 -> 902,
-// non-causal 1025 -> 1047, 1 x 32 x 8192 causal 1050 -> 1072; at 1 x 32 x 32768
-// causal (256 query tiles per key tile) the two are level.
-static bool bwd_persistent_pays(int Nq, int Nk, bool causal, int window) {
-  const int Tk = (Nk + kBwdBc - 1) / kBwdBc;
-  for (int kt = 0; kt < Tk; ++kt) {  // the widest ranges are at the start (causal) or inside (window)
-    int lo = 0, hi = -1;
-    query_tile_range(kt, bwd_br(128), kBwdBc, Nq, Nk, causal, window, &lo, &hi);
-    if (hi - lo + 1 > 128) return false;
-    if (window == 0) break;  // without a window the first key tile is seen by the most
-  }
-  return true;
-}
-
-// The backward form that runs: the split (bwd_split), made persistent at d = 128
-// where that pays.
+// The backward form that runs: the split (bwd_split), persistent at d = 128.  Measured
+// on GB300 (backward TFLOP/s, one CTA per key tile -> persistent, both forms taking
+// their per-step code from one header, calls of the two interleaved): 1 x 32 x 32768
+// causal (256 query tiles per key tile) 1140 -> 1149, 1 x 32 x 8192 causal 1063 ->
+// 1096, 2 x 16 x 4096 causal 898 -> 938.  (Mask and sizes no longer enter the choice;
+// the arguments stay for the forward's rule and for callers.)
 static int bwd_form_for(int d, int Nq, int Nk, bool causal, int window, int setting) {
+  (void)Nq, (void)Nk, (void)causal, (void)window;
   const int split = bwd_split(d, setting);
-  if (split == 1 && d == 128 && setting == 0 && bwd_persistent_pays(Nq, Nk, causal, window)) return 3;
+  if (split == 1 && d == 128 && setting == 0) return 3;
   return split;
 }
 

@@ -268,9 +268,8 @@ fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter);
  *   3: form 1 with one CTA per SM taking key tiles from a queue, consecutive
  *      tiles overlapped (d = 128; other d run form 1 in its place; the same
  *      1024 work counters rule as fa_debug_set_fwd_form's form 3);
- *   0: the library's default, chosen by measurement on GB300: form 2 at d = 64;
- *      at d = 128 form 3, or form 1 when some key tile is seen by more than 128
- *      query tiles.
+ *   0: the library's default, chosen by measurement on GB300: form 2 at d = 64,
+ *      form 3 at d = 128.
  * d = 32 always runs form 1.  Process-wide setting; FA_ERR_INVALID_ARG for
  * other values.
  */

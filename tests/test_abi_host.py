@@ -178,13 +178,13 @@ def test_forward_form_switch(fa_lib):
 
 
 @pytest.mark.parametrize("Nq,Nk,d,causal,window,fwd,bwd", [
-    (32768, 32768, 128, 1, 0, 1, 1),   # 256 key tiles per query tile: the one-tile kernels
-    (32768, 32768, 128, 0, 0, 1, 1),
+    (32768, 32768, 128, 1, 0, 1, 3),   # 256 key tiles per query tile: the one-tile forward
+    (32768, 32768, 128, 0, 0, 1, 3),
     (16384, 16384, 128, 1, 0, 3, 3),   # up to 128: persistent
     (8192, 8192, 128, 1, 0, 3, 3),
     (4096, 4096, 128, 0, 0, 3, 3),
     (8192, 8192, 128, 1, 1024, 3, 3),  # a window: few tiles per row
-    (2048, 32768, 128, 1, 0, 1, 3),    # prefill: long rows, short key-tile loops
+    (2048, 32768, 128, 1, 0, 1, 3),    # prefill: long rows; the backward is persistent at d = 128
     (1024, 1024, 64, 1, 0, 3, 2),      # d = 64: persistent forward, two-kernel backward
     (256, 256, 32, 0, 0, 3, 1),        # d = 32: persistent forward, one-kernel backward
 ])
