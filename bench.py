@@ -42,7 +42,7 @@ UNIT = "TFLOP/s"
 # backward main kernel on the very long causal shape, from the ncu capture of this
 # kernel on that shape; valid for the kernel as captured (set to None whenever the
 # kernel changes).
-_TRAFFIC = {("vlong_1x32x32768x128", True): 1621075712 + 1022706944}
+_TRAFFIC = {("vlong_1x32x32768x128", True): 1621346474 + 1022888448}
 
 
 def _peaks():
@@ -357,9 +357,9 @@ def run_ours(args):
     fwd_tflops = flops_f * args.steps / (fwd_ms / 1e3) / 1e12
     bwd_kernel_tflops = flops_b * args.steps / (bwd_k_ms / 1e3) / 1e12
     fwd_kernel_tflops = flops_f * args.steps / (fwd_k_ms / 1e3) / 1e12
-    st_forms, f_form, b_form = fa.fa_selected_forms(r.Nq, r.Nk, w.d, causal, args.window)
-    bwd_kernel = {1: "bwd_d128_kernel" if w.d == 128 else "bwd_kernel", 2: "bwd_kv_kernel + bwd_q_kernel",
-                  3: "bwd_d128p_kernel"}.get(b_form, "?") if st_forms == fa.FA_OK else "?"
+    st_forms, f_form, b_form = fa.fa_selected_forms(w.B, w.H, r.Nq, r.Nk, w.d, causal, args.window)
+    bwd_kernel = {1: "bwd_tile_kernel" if w.d >= 64 else "bwd_kernel", 2: "bwd_kv_kernel + bwd_q_kernel",
+                  3: "bwd_persist_kernel"}.get(b_form, "?") if st_forms == fa.FA_OK else "?"
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",

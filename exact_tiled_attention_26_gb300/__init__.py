@@ -69,7 +69,7 @@ _sig = {
     "fa_debug_set_tile_counter": (_i, [_vp]),
     "fa_debug_set_bwd_split": (_i, [_i]),
     "fa_debug_set_fwd_form": (_i, [_i]),
-    "fa_selected_forms": (_i, [_i] * 5 + [ctypes.POINTER(_i)] * 2),
+    "fa_selected_forms": (_i, [_i] * 7 + [ctypes.POINTER(_i)] * 2),
     "fa_debug_bwd_plan": (_i, [_i] * 7 + [ctypes.POINTER(_i), ctypes.POINTER(_sz)]),
     "fa_debug_set_kernel_events": (_i, [_i, _vp, _vp]),
     "fa_poll_device_error": (_i, [_vp, ctypes.POINTER(_i)]),
@@ -169,10 +169,10 @@ def fa_debug_set_fwd_form(form):
     return lib.fa_debug_set_fwd_form(form)
 
 
-def fa_selected_forms(Nq, Nk, d, causal, window):
+def fa_selected_forms(B, H, Nq, Nk, d, causal, window):
     """(status, forward form, backward form) the library would run for these sizes and mask."""
     f, b = _i(0), _i(0)
-    st = lib.fa_selected_forms(Nq, Nk, d, int(bool(causal)), window, ctypes.byref(f), ctypes.byref(b))
+    st = lib.fa_selected_forms(B, H, Nq, Nk, d, int(bool(causal)), window, ctypes.byref(f), ctypes.byref(b))
     return st, f.value, b.value
 
 

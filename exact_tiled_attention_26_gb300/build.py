@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libfa_gb300.so")
-SOURCES = ["api.cu", "fwd.cu", "fwd_pp.cu", "fwd_persist.cu", "bwd.cu", "bwd128.cu", "bwd128p.cu", "bwd2k.cu", "aux.cu", "bwd_noalloc.cu", "host_step.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_pp.cu", "fwd_persist.cu", "bwd.cu", "bwd_tile.cu", "bwd_persist.cu", "bwd2k.cu", "aux.cu", "bwd_noalloc.cu", "host_step.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]

@@ -37,8 +37,15 @@ KernelEvents kernel_events(int which) {
   std::lock_guard<std::mutex> lk(g_kev_mu);
   return g_kev[which];
 }
-constexpr int kDefaultBwdSplitD128 = 1;  // chosen by measurement on GB300
-constexpr int kDefaultBwdSplitD64 = 2;  // two kernels: faster at d = 64 (measured)
+constexpr int kDefaultBwdSplitD128 = 1;  // chosen by measurement on GB300 (then persistent: bwd_form_for)
+// d = 64: the persistent one-kernel form once the problem has more visible tile
+// pairs than this (about 20 per SM), else the two kernels, whose shorter steps and
+// missing workspace passes (clear, dQ convert) win on small problems.  Measured on
+// GB300, backward call in us (two kernels / persistent): 4x8x1024 causal, 1152 pairs,
+// 43.9 / 47.9; 4x8x1024, 2048 pairs, 58.8 / 60.5; 4x8x2048 causal, 4352 pairs,
+// 103.7 / 97.3; 8x16x1024 causal, 4608 pairs, 138.8 / 113.8; 1x32x8192 causal,
+// 66560 pairs, 1058 / 957.
+constexpr long long kD64PersistentMinPairs = 3072;
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -270,9 +277,8 @@ fa_status fa_bwd_preprocess(const void* O, const void* dO, float* D, int B, int 
 // fp32 workspace, 2 = two kernels (key tiles for dK, dV; query tiles for dQ).
 static int bwd_split(int d, int setting) {
   if (d != 128 && d != 64) return 1;
-  if (setting == 3) return d == 128 ? 3 : 1;  // the persistent form exists at d = 128
   if (setting != 0) return setting;
-  return d == 128 ? kDefaultBwdSplitD128 : kDefaultBwdSplitD64;
+  return kDefaultBwdSplitD128;
 }
 
 // The backward form that runs: the split (bwd_split), persistent at d = 128.  Measured
@@ -281,11 +287,12 @@ static int bwd_split(int d, int setting) {
 // causal (256 query tiles per key tile) 1140 -> 1149, 1 x 32 x 8192 causal 1063 ->
 // 1096, 2 x 16 x 4096 causal 898 -> 938.  (Mask and sizes no longer enter the choice;
 // the arguments stay for the forward's rule and for callers.)
-static int bwd_form_for(int d, int Nq, int Nk, bool causal, int window, int setting) {
-  (void)Nq, (void)Nk, (void)causal, (void)window;
+static int bwd_form_for(int BH, int d, int Nq, int Nk, bool causal, int window, int setting) {
   const int split = bwd_split(d, setting);
-  if (split == 1 && d == 128 && setting == 0) return 3;
-  return split;
+  if (setting != 0 || (d != 128 && d != 64)) return split;
+  if (d == 128) return 3;
+  const long long pairs = static_cast<long long>(BH) * fa_tile_pairs_ex(Nq, Nk, d, causal ? 1 : 0, window, 1);
+  return pairs > kD64PersistentMinPairs ? 3 : 2;
 }
 
 // The backward form and the workspace it needs, both from one snapshot of the
@@ -296,7 +303,7 @@ struct BwdPlan {
   size_t need;
 };
 static BwdPlan bwd_plan(int B, int H, int Nq, int Nk, int d, bool causal, int window, bool empty, int setting) {
-  BwdPlan p{bwd_form_for(d, Nq, Nk, causal, window, setting), 0};
+  BwdPlan p{bwd_form_for(B * H, d, Nq, Nk, causal, window, setting), 0};
   if (!empty && p.form != 2) p.need = static_cast<size_t>(B) * H * Nq * d * sizeof(float);
   return p;
 }
@@ -323,13 +330,14 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, int causal) {
   return fa_bwd_workspace_size_ex(B, H, N, N, d, causal, 0);
 }
 
-fa_status fa_selected_forms(int Nq, int Nk, int d, int causal, int window, int* fwd_form, int* bwd_form) {
+fa_status fa_selected_forms(int B, int H, int Nq, int Nk, int d, int causal, int window, int* fwd_form,
+                            int* bwd_form) {
   bool empty = false;
   if (!fwd_form || !bwd_form) return FA_ERR_INVALID_ARG;
-  const fa_status st = check_mask_shape(1, 1, Nq, Nk, d, causal, window, &empty);
+  const fa_status st = check_mask_shape(B, H, Nq, Nk, d, causal, window, &empty);
   if (st != FA_OK) return st;
   *fwd_form = fwd_form_for(d, Nq, Nk, causal != 0, window, g_fwd_form.load());
-  *bwd_form = bwd_form_for(d, Nq, Nk, causal != 0, window, g_bwd_split.load());
+  *bwd_form = bwd_form_for(B * H, d, Nq, Nk, causal != 0, window, g_bwd_split.load());
   return FA_OK;
 }
 
@@ -391,9 +399,10 @@ fa_status fa_bwd_ex(const void* Q, const void* K, const void* V, const void* O, 
     if (st == FA_OK && ev.stop != nullptr && cudaEventRecord(ev.stop, stream) != cudaSuccess) return FA_ERR_CUDA;
     return st;
   }
-  if (cudaMemsetAsync(workspace, 0, need, stream) != cudaSuccess) return FA_ERR_CUDA;
+  st = launch_zero(workspace, need, stream);
+  if (st != FA_OK) return st;
   if (ev.start != nullptr && cudaEventRecord(ev.start, stream) != cudaSuccess) return FA_ERR_CUDA;
-  st = plan.form == 3 ? launch_bwd_d128_persist(a) : launch_bwd(a);
+  st = plan.form == 3 ? launch_bwd_persist(a) : launch_bwd(a);
   if (st != FA_OK) return st;
   if (ev.stop != nullptr && cudaEventRecord(ev.stop, stream) != cudaSuccess) return FA_ERR_CUDA;
   return launch_dq_convert(static_cast<const float*>(workspace), dQ, static_cast<long long>(B) * H * Nq * d, scale,

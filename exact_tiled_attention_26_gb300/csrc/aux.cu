@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const __nv_bfloat16* __
   const int sub = lane / LPR, part = lane % LPR;
   const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  pdl_wait();  // O is the forward's output
   for (long long base = warp_id * RPW * UNR; base < rows; base += nwarps * RPW * UNR) {
     uint4 a[UNR], b[UNR];
 #pragma unroll
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
                                                          __nv_bfloat16* __restrict__ dst, long long n8,
                                                          float scale) {
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  pdl_wait();  // src is complete once the backward kernel has ended
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += stride) {
     const uint4 lo = ld_stream_v4(src + 8 * i);
     const uint4 hi = ld_stream_v4(src + 8 * i + 4);
@@ -86,6 +88,14 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
     out.w = pack_bf16x2(__uint_as_float(hi.z) * scale, __uint_as_float(hi.w) * scale);
     *reinterpret_cast<uint4*>(dst + 8 * i) = out;
   }
+}
+
+// The fp32 dQ workspace cleared before the backward kernel reduces into it.
+__global__ void __launch_bounds__(256) zero_kernel(uint4* __restrict__ p, long long n16) {
+  pdl_trigger();  // the backward kernel may start its loads now; it waits before reducing
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
 enum : int { SITE_PROBE = 0x301, SITE_SELFTEST = 0x401 };
@@ -247,12 +257,23 @@ fa_status launch_preprocess(const void* O, const void* dO, float* D, long long r
   if (blocks < 1) blocks = 1;
   const auto* o = static_cast<const __nv_bfloat16*>(O);
   const auto* g = static_cast<const __nv_bfloat16*>(dO);
+  const dim3 grid(static_cast<unsigned>(blocks));
+  cudaError_t e = cudaSuccess;
   switch (d) {
-    case 32: preprocess_kernel<32><<<static_cast<unsigned>(blocks), 256, 0, s>>>(o, g, D, rows); break;
-    case 64: preprocess_kernel<64><<<static_cast<unsigned>(blocks), 256, 0, s>>>(o, g, D, rows); break;
-    case 128: preprocess_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, s>>>(o, g, D, rows); break;
+    case 32: e = launch_pdl(preprocess_kernel<32>, grid, dim3(256), 0, s, o, g, D, rows); break;
+    case 64: e = launch_pdl(preprocess_kernel<64>, grid, dim3(256), 0, s, o, g, D, rows); break;
+    case 128: e = launch_pdl(preprocess_kernel<128>, grid, dim3(256), 0, s, o, g, D, rows); break;
     default: return FA_ERR_UNSUPPORTED;
   }
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status launch_zero(void* p, size_t bytes, cudaStream_t s) {
+  const long long n16 = static_cast<long long>(bytes / 16);
+  long long blocks = (n16 + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks < 1) blocks = 1;
+  zero_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<uint4*>(p), n16);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -261,9 +282,9 @@ fa_status launch_dq_convert(const float* dQacc, void* dQ, long long n, float sca
   long long blocks = (n8 + 255) / 256;
   if (blocks > 152 * 16) blocks = 152 * 16;
   if (blocks < 1) blocks = 1;
-  dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(dQacc, static_cast<__nv_bfloat16*>(dQ), n8,
-                                                                   scale);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(dq_convert_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s, dQacc,
+                                   static_cast<__nv_bfloat16*>(dQ), n8, scale);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 fa_status launch_timeout_probe(int limit_us, cudaStream_t s, int* status) {

@@ -1,5 +1,6 @@
-// Backward pass of exact tiled attention on sm_103a: main kernel for head sizes
-// 32 and 64 (head size 128 has its own pipelined kernel in bwd128.cu).
+// Backward pass of exact tiled attention on sm_103a: main kernel for head size 32
+// (head sizes 64 and 128 run the pipelined kernels of bwd_tile.cu and bwd_persist.cu;
+// the d = 128 branches below are this first version's and are not instantiated).
 //
 // "CS336 Assignment 2 notes" §1.4, Equations 13-19, with the key/value tiles
 // in the outer loop (kernel 1 of the notes' two-kernel scheme).  One CTA owns
@@ -382,8 +383,8 @@ fa_status launch_bwd_t(const BwdLaunch& a) {
 fa_status launch_bwd(const BwdLaunch& a) {
   switch (a.d) {
     case 32: return a.causal ? launch_bwd_t<32, true>(a) : launch_bwd_t<32, false>(a);
-    case 64: return a.causal ? launch_bwd_t<64, true>(a) : launch_bwd_t<64, false>(a);
-    case 128: return launch_bwd_d128(a);  // software-pipelined kernel of bwd128.cu
+    case 64:
+    case 128: return launch_bwd_tile(a);  // the tensor-core pipeline of bwd_tile.cu
     default: return FA_ERR_UNSUPPORTED;
   }
 }

@@ -1,8 +1,9 @@
-// The per-step work of every role of the head-size-128 backward ("CS336 Assignment 2
-// notes" §1.4, Equations 13-19, key/value tiles outer), shared by the kernel with one
-// CTA per key tile (bwd128.cu) and the persistent kernel (bwd128p.cu).  Both kernels
-// lay out shared and tensor memory the same way and number the per-step barriers the
-// same way (the constants below); they differ only in how they walk units of work.
+// The per-step work of every role of the tensor-core backward at head sizes 64 and 128
+// ("CS336 Assignment 2 notes" §1.4, Equations 13-19, key/value tiles outer), shared by
+// the kernel with one CTA per key tile (bwd_tile.cu) and the persistent kernel
+// (bwd_persist.cu).  Both kernels lay out shared and tensor memory the same way and
+// number the per-step barriers the same way (the constants below); they differ only in
+// how they walk units of work.
 //
 // One step processes query tile i against the CTA's key tile j, keys on the 128
 // tensor-memory lanes:
@@ -15,14 +16,20 @@
 //   dQ_i^T = K^T dS^T                    (UMMA, over the dP^T columns)
 //   dQ_i += dQ_i^T, added from registers into the fp32 workspace with
 //           coalesced reductions in L2                             Eq 18
-// Tensor memory (512 columns): dK 128 | dV 128 | two 128-column regions that take
-// turns.  Step g keeps S^T in region g % 2; there query half h (64 queries) overwrites
+// Every UMMA has M = 128 and N = 128 or d.  At d = 64 the dQ^T product keeps M = 128:
+// its A operand K^T is read from a K tile stored twice (the second 64-column chunk a
+// copy of the first), so tensor-memory lanes 64..127 repeat d = 0..63 -- the
+// tensor pipe takes an M = 64 product no faster, and the result keeps the
+// M = 128 lane layout.
+// Tensor memory (512 columns): dK 128 | dV 128 (d columns of each used) | two
+// 128-column regions that take turns.  Step g keeps S^T in region g % 2; there query half h (64 queries) overwrites
 // its own S^T with its bf16 P^T (columns 64h .. 64h+31) and dS^T (64h+32 .. 64h+63),
 // and once dV and dK have read those, dQ_g^T is formed over the whole region.  dP^T of
 // step g goes to region (g + 1) % 2, which held dQ^T of step g-1.
 //
 // `g` is the CTA's step count: it picks the Q, dO stage, the tensor-memory regions and
-// every barrier phase, and runs on across units in the persistent kernel.
+// every barrier phase, and runs on across units in the persistent kernel.  `kvb` is the
+// K, V buffer of the step's unit (the persistent kernel keeps two at d = 64).
 #pragma once
 
 #include <type_traits>
@@ -30,13 +37,13 @@
 #include "ptx.cuh"
 
 namespace fa {
-namespace b128 {
+namespace bsteps {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int D = 128, BN = 128, BM = 128;
+constexpr int BN = 128, BM = 128;
 constexpr int NCOMP = 256;  // element-wise threads (warps 4..11)
 constexpr int NDQ = 128;    // dQ drain threads (warps 12..15)
-constexpr int TILE = 128 * 128 * 2;  // one 128 x 128 bf16 tile (two 64-column chunks)
+constexpr int CHUNK = 128 * 64 * 2;  // 128 rows x 64 bf16 columns (one 128-byte swizzle span)
 // Per-step barriers (the kernels add their own from 17 on).
 enum : int {
   B_QFULL = 1, B_QEMPTY = 3, B_SFULL = 5, B_DPFULL = 6,
@@ -48,14 +55,32 @@ constexpr int OFF_BAR = 0;
 constexpr int OFF_LD = 256;  // 2 stages x (-L*log2 e [128], D [128])
 constexpr int LD_BYTES = 2 * BM * 4;
 constexpr int SMALL = OFF_LD + 2 * LD_BYTES;
-// 1 KiB-aligned tiles after the small region; Q, dO: stage s adds s * 2 * TILE
-constexpr int T_K = 0, T_V = TILE, T_Q = 2 * TILE, T_DO = 3 * TILE;
-constexpr int T_DS = 6 * TILE;  // dS^T [128 keys][128 queries]
-constexpr int TILES = 7 * TILE;  // 224 KiB
-constexpr int SMEM = 232448;    // the per-block maximum
+constexpr int SMEM_MAX = 232448;  // the per-block maximum
 constexpr int TM_DK = 0, TM_DV = 128, TM_R = 256, TM_COLS = 512;
-// with a 1 KiB-aligned base the tiles start at 3 KiB and end exactly at the limit
-static_assert(SMALL <= 3072 && 3072 + TILES <= SMEM, "shared memory budget");
+
+// Shared-memory layout at head size D with NKV K, V buffers, 1 KiB-aligned tiles after
+// the small region.  Every 128-row tile is stored in 64-column chunks of CHUNK bytes.
+template <int D, int NKV_>
+struct Lay {
+  static_assert(D == 64 || D == 128, "head size");
+  static constexpr int NKV = NKV_;
+  static constexpr int TQ = 128 * D * 2;  // a Q, dO or V tile
+  static constexpr int TK = 2 * CHUNK;    // K: two chunks (at D = 64 the second is a copy)
+  static constexpr int KVB = TK + TQ;     // one K, V buffer
+  static constexpr int T_Q = NKV_ * KVB;   // Q, dO of stage s at T_Q + s * 2 TQ (+ TQ for dO)
+  static constexpr int T_DS = T_Q + 4 * TQ;  // dS^T [128 keys][128 queries]
+  static constexpr int TILES = T_DS + 2 * CHUNK;
+  static constexpr int SMEM = 3072 + TILES;  // with a 1 KiB-aligned base the tiles start at 3 KiB
+  static_assert(SMALL <= 3072 && SMEM <= SMEM_MAX, "shared memory budget");
+  static FA_DEV uint32_t k(uint32_t tb, int b) { return tb + b * KVB; }
+  static FA_DEV uint32_t v(uint32_t tb, int b) { return tb + b * KVB + TK; }
+  static FA_DEV uint32_t q(uint32_t tb, int s) { return tb + T_Q + s * 2 * TQ; }
+  static FA_DEV uint32_t dO(uint32_t tb, int s) { return tb + T_Q + s * 2 * TQ + TQ; }
+};
+// The layouts the kernels use: one K, V buffer at d = 128 (224 KiB of tiles), two at
+// d = 64 (192 KiB).
+template <int D>
+using LayFor = Lay<D, D == 128 ? 1 : 2>;
 
 // What every role needs: shared-window addresses of the small region and the tiles,
 // generic pointers to the same, the tensor-memory base and the wait guard.
@@ -71,6 +96,7 @@ struct Ctx {
 // Producer (whole warp): Q_i, dO_i of query tile rows q0 .. q0+127 of head bh into
 // stage g % 2 (once the dK product of step g-2 has released it), and -L log2 e, D of
 // those rows into shared memory (rows past Nq get -L log2 e = -inf, so their P is 0).
+template <class LY>
 FA_DEV bool produce_step(const Ctx& x, const CUtensorMap* tmQ, const CUtensorMap* tmdO, const float* Lg,
                          const float* Dg, size_t row0, int Nq, int q0, int bh, int g, int lane, int site) {
   const int s = g & 1;
@@ -84,10 +110,10 @@ FA_DEV bool produce_step(const Ctx& x, const CUtensorMap* tmQ, const CUtensorMap
   }
   if (!mbar_wait_warp(x.bar(B_QEMPTY + s), ((g >> 1) & 1) ^ 1, x.guard, site)) return false;
   if (lane == 0) {
-    mbar_expect_tx(x.bar(B_QFULL + s), 2 * TILE);
-    for (int c = 0; c < 2; ++c) {
-      tma_load_3d(x.tb + T_Q + s * 2 * TILE + c * 128 * 128, tmQ, x.bar(B_QFULL + s), c * 64, q0, bh);
-      tma_load_3d(x.tb + T_DO + s * 2 * TILE + c * 128 * 128, tmdO, x.bar(B_QFULL + s), c * 64, q0, bh);
+    mbar_expect_tx(x.bar(B_QFULL + s), 2 * LY::TQ);
+    for (int c = 0; c < LY::TQ / CHUNK; ++c) {
+      tma_load_3d(LY::q(x.tb, s) + c * CHUNK, tmQ, x.bar(B_QFULL + s), c * 64, q0, bh);
+      tma_load_3d(LY::dO(x.tb, s) + c * CHUNK, tmdO, x.bar(B_QFULL + s), c * 64, q0, bh);
     }
   }
   float* Ls = reinterpret_cast<float*>(x.small + OFF_LD + s * LD_BYTES);
@@ -101,26 +127,28 @@ FA_DEV bool produce_step(const Ctx& x, const CUtensorMap* tmQ, const CUtensorMap
 }
 
 // UMMA issuer A (one thread): S^T = K Q^T into region g % 2, dP^T = V dO^T into the
-// other region.  K and V must be in shared memory.
-FA_DEV bool issue_s_dp(const Ctx& x, int g, int site) {
+// other region.  K and V (buffer kvb) must be in shared memory.
+template <class LY>
+FA_DEV bool issue_s_dp(const Ctx& x, int g, int kvb, int site) {
   constexpr uint32_t idKK = idesc_bf16(128, 128, false, false);  // K-major x K-major
+  constexpr int KS = LY::TQ / (128 * 32);                         // k-steps of 16 over d
   const int s = g & 1;
-  const uint32_t kb = x.tb + T_K, vb = x.tb + T_V;
-  const uint32_t qb = x.tb + T_Q + s * 2 * TILE, db = x.tb + T_DO + s * 2 * TILE;
+  const uint32_t kb = LY::k(x.tb, kvb), vb = LY::v(x.tb, kvb);
+  const uint32_t qb = LY::q(x.tb, s), db = LY::dO(x.tb, s);
   const uint32_t rs = x.tmem + TM_R + 128 * s, rd = x.tmem + TM_R + 128 * (s ^ 1);
   if (!mbar_wait(x.bar(B_QFULL + s), (g >> 1) & 1, x.guard, site)) return false;
   // region s held dP^T of the previous step: every element-wise thread has read it
   if (g > 0 && !mbar_wait(x.bar(B_DPCONS), (g - 1) & 1, x.guard, site)) return false;
   tc_fence_after();
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
+  for (int ks = 0; ks < KS; ++ks)
     mma_ss(rs, sdesc_kmajor<128, 128>(kb, ks), sdesc_kmajor<128, 128>(qb, ks), idKK, ks > 0);
   mma_commit(x.bar(B_SFULL));
   // region s^1 ended the previous step holding its dQ^T: the drain warps have read it
   if (g > 0 && !mbar_wait(x.bar(B_DQCONS), (g - 1) & 1, x.guard, site)) return false;
   tc_fence_after();
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks)
+  for (int ks = 0; ks < KS; ++ks)
     mma_ss(rd, sdesc_kmajor<128, 128>(vb, ks), sdesc_kmajor<128, 128>(db, ks), idKK, ks > 0);
   mma_commit(x.bar(B_DPFULL));
   return true;
@@ -131,12 +159,13 @@ FA_DEV bool issue_s_dp(const Ctx& x, int g, int site) {
 // and dK have read its P^T and dS^T.  first: the unit's first step (the accumulators
 // start from zero).  S^T and dP^T of the step are complete before the element-wise
 // warps signal P and dS ready, so this thread's commits cover every reader of Q, dO.
-FA_DEV bool issue_dv_dk_dq(const Ctx& x, int g, bool first, int site) {
-  constexpr uint32_t idTN = idesc_bf16(128, 128, false, true);  // A in TMEM x N-major B
-  constexpr uint32_t idMN = idesc_bf16(128, 128, true, true);   // K^T (M-major) x dS^T (N-major)
+template <class LY>
+FA_DEV bool issue_dv_dk_dq(const Ctx& x, int g, int kvb, bool first, int site) {
+  constexpr uint32_t idTN = idesc_bf16(128, LY::TQ / 256, false, true);  // A in TMEM x N-major B (N = d)
+  constexpr uint32_t idMN = idesc_bf16(128, 128, true, true);            // K^T (M-major) x dS^T (N-major)
   const int s = g & 1;
-  const uint32_t kb = x.tb + T_K, dsb = x.tb + T_DS;
-  const uint32_t qb = x.tb + T_Q + s * 2 * TILE, db = x.tb + T_DO + s * 2 * TILE;
+  const uint32_t kb = LY::k(x.tb, kvb), dsb = x.tb + LY::T_DS;
+  const uint32_t qb = LY::q(x.tb, s), db = LY::dO(x.tb, s);
   const uint32_t rs = x.tmem + TM_R + 128 * s;
   // dV += P^T dO.  Query block ks (16 queries) is in half ks/4, sub-chunk (ks%4)/2; its
   // bf16 P^T sits in columns 64 (ks/4) + 8 (ks%4).  Sub-chunk 0 (blocks 0,1,4,5) is
@@ -176,27 +205,34 @@ FA_DEV bool issue_dv_dk_dq(const Ctx& x, int g, bool first, int site) {
   return true;
 }
 
-// dQ drain (warp qw of warps 12..15: lane quarter qw, i.e. d = 32 qw + lane): takes all
-// 128 columns of dQ_g^T out of tensor memory at once, frees them, then adds them into
-// the fp32 workspace from registers (each warp access covers 32 consecutive d of one
-// query row, 128 bytes).  dst: workspace row q0 (of nq <= 128 valid rows), column d.
-FA_DEV bool drain_step(const Ctx& x, int g, float* dst, int nq, int qw, int site) {
+// dQ drain (warp qw of warps 12..15, lane quarter qw): takes its columns of dQ_g^T out
+// of tensor memory at once, frees them, then adds them into the fp32 workspace from
+// registers (each warp access covers 32 consecutive d of one query row, 128 bytes).
+// d = 128: d = 32 qw + lane, all 128 queries.  d = 64 (lanes 64..127 repeat 0..63):
+// d = 32 (qw % 2) + lane, queries 64 (qw / 2) .. +63.  tile: workspace row q0 of the
+// step's query tile (nq <= 128 valid rows).
+template <int D>
+FA_DEV bool drain_step(const Ctx& x, int g, float* tile, int nq, int qw, int lane, int site) {
+  constexpr int NQ = D == 128 ? 128 : 64;  // queries per drain thread
+  const int qb = D == 128 ? 0 : 64 * (qw >> 1);
+  float* dst = tile + static_cast<size_t>(qb) * D + (D == 128 ? qw : (qw & 1)) * 32 + lane;
+  const int nv = nq - qb;  // valid queries of this thread's range
   const uint32_t tl = x.tmem + (static_cast<uint32_t>(qw * 32) << 16);
   if (!mbar_wait_warp(x.bar(B_DQFULL), g & 1, x.guard, site)) return false;
   tc_fence_after();
-  uint32_t r[128];
+  uint32_t r[NQ];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) tmem_ld32(tl + TM_R + 128 * (g & 1) + 32 * c, r + 32 * c);
-  tmem_ld_wait<128>(r);
+  for (int c = 0; c < NQ / 32; ++c) tmem_ld32(tl + TM_R + 128 * (g & 1) + qb + 32 * c, r + 32 * c);
+  tmem_ld_wait<NQ>(r);
   tc_fence_before();
   mbar_arrive(x.bar(B_DQCONS));
-  if (nq >= BM) {
+  if (nv >= NQ) {
 #pragma unroll
-    for (int q = 0; q < BM; ++q) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(r[q]));
+    for (int q = 0; q < NQ; ++q) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(r[q]));
   } else {
 #pragma unroll
-    for (int q = 0; q < BM; ++q)
-      if (q < nq) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(r[q]));
+    for (int q = 0; q < NQ; ++q)
+      if (q < nv) atomicAdd(dst + static_cast<size_t>(q) * D, __uint_as_float(r[q]));
   }
   return true;
 }
@@ -204,7 +240,7 @@ FA_DEV bool drain_step(const Ctx& x, int g, float* dst, int nq, int qw, int site
 // Element-wise warps (warp w of 4..11: lane quarter qw = w % 4, query half h = (w-4)/4;
 // one key row per thread): P^T and dS^T of step g, key tile kt (this thread's key
 // row kr), query tile qt.  off = Nk - Nq (query q sits at q + off).
-template <bool CAUSAL>
+template <class LY, bool CAUSAL>
 FA_DEV bool ew_step(const Ctx& x, int g, int kt, int qt, int Nk, int off, int window, float c_log2, int qw, int h,
                     int lane, int site) {
   const int s = g & 1;
@@ -267,7 +303,7 @@ FA_DEV bool ew_step(const Ctx& x, int g, int kt, int qt, int Nk, int off, int wi
   // ---- dS^T = P^T (dP^T - D), from the same bf16 P that enters dV; two sub-chunks
   if (!mbar_wait_warp(x.bar(B_DPFULL), g & 1, x.guard, site)) return false;
   tc_fence_after();
-  uint8_t* row = x.tiles + T_DS + h * (128 * 128) + kr * 128;
+  uint8_t* row = x.tiles + LY::T_DS + h * CHUNK + kr * 128;
   // all of this thread's dP^T out of tensor memory first, so that S^T of the next step
   // can be formed in its region while dS is computed
   uint32_t rdp[64];
@@ -312,37 +348,43 @@ FA_DEV bool ew_step(const Ctx& x, int g, int kt, int qt, int Nk, int off, int wi
 }
 
 // Element-wise epilogue, first half: this thread's key row of dK (times scale) and dV,
-// d columns 64h .. 64h+63, out of tensor memory as packed bf16 ([dK | dV] x 32 pairs);
-// zero when no query saw these keys (the accumulators were never written).
-FA_DEV void ew_load_dk_dv(const Ctx& x, int qw, int h, float scale, bool none, uint32_t (&outp)[64]) {
+// d columns (D/2) h .. (D/2) h + D/2 - 1, out of tensor memory as packed bf16
+// ([dK | dV] x D/4 pairs); zero when no query saw these keys (the accumulators were
+// never written).
+template <int D>
+FA_DEV void ew_load_dk_dv(const Ctx& x, int qw, int h, float scale, bool none, uint32_t (&outp)[D / 2]) {
+  constexpr int HW = D / 2;  // d columns per query half
   const uint32_t tl = x.tmem + (static_cast<uint32_t>(qw * 32) << 16);
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const float f = t == 0 ? scale : 1.f;
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < HW / 32; ++c) {
       uint32_t r[32];
-      tmem_ld32(tl + (t == 0 ? TM_DK : TM_DV) + 64 * h + 32 * c, r);
+      tmem_ld32(tl + (t == 0 ? TM_DK : TM_DV) + HW * h + 32 * c, r);
       tmem_ld_wait<32>(r);
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        outp[32 * t + 16 * c + i] =
+        outp[(HW / 2) * t + 16 * c + i] =
             none ? 0u : pack_bf16x2(__uint_as_float(r[2 * i]) * f, __uint_as_float(r[2 * i + 1]) * f);
     }
   }
 }
 
-// Second half: the row into dK and dV (row `key` of the rows starting at krow0).
-FA_DEV void ew_store_dk_dv(const uint32_t (&outp)[64], __nv_bfloat16* dK, __nv_bfloat16* dV, size_t krow, int h) {
+// Second half: the row into dK and dV (row krow of [B*H*Nk, D]).
+template <int D>
+FA_DEV void ew_store_dk_dv(const uint32_t (&outp)[D / 2], __nv_bfloat16* dK, __nv_bfloat16* dV, size_t krow,
+                           int h) {
+  constexpr int HW = D / 2;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    uint4* d4 = reinterpret_cast<uint4*>((t == 0 ? dK : dV) + krow * D + 64 * h);
+    uint4* d4 = reinterpret_cast<uint4*>((t == 0 ? dK : dV) + krow * D + HW * h);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      d4[i] = make_uint4(outp[32 * t + 4 * i], outp[32 * t + 4 * i + 1], outp[32 * t + 4 * i + 2],
-                         outp[32 * t + 4 * i + 3]);
+    for (int i = 0; i < HW / 8; ++i)
+      d4[i] = make_uint4(outp[(HW / 2) * t + 4 * i], outp[(HW / 2) * t + 4 * i + 1], outp[(HW / 2) * t + 4 * i + 2],
+                         outp[(HW / 2) * t + 4 * i + 3]);
   }
 }
 
-}  // namespace b128
+}  // namespace bsteps
 }  // namespace fa

@@ -1,12 +1,12 @@
-// Backward pass, head size 128: one CTA per key tile.
+// Backward pass, head sizes 64 and 128: one CTA per key tile.
 //
-// Same mathematics as bwd.cu ("CS336 Assignment 2 notes" §1.4, Equations 13-19,
-// key/value tiles outer): one CTA owns 128 keys of one (batch, head); K_j and V_j
-// stay in shared memory while the CTA walks the visible 128-row query tiles i.  The
-// per-step work of every role (the five UMMAs, the element-wise P^T and dS^T, the dQ
-// drain) is in bwd128_steps.cuh, shared with the persistent kernel (bwd128p.cu);
-// this file walks a single unit of work per CTA.  The softmax scale of Eq 18-19 is
-// applied to dK at the end and to dQ by the convert pass.
+// "CS336 Assignment 2 notes" §1.4, Equations 13-19, key/value tiles outer: one CTA
+// owns 128 keys of one (batch, head); K_j and V_j stay in shared memory while the CTA
+// walks the visible 128-row query tiles i.  The per-step work of every role (the five
+// UMMAs, the element-wise P^T and dS^T, the dQ drain) is in bwd_steps.cuh, shared with
+// the persistent kernel (bwd_persist.cu); this file walks a single unit of work per
+// CTA.  The softmax scale of Eq 18-19 is applied to dK at the end and to dQ by the
+// convert pass.
 //
 // Every UMMA is M = 128, N = 128 (narrower UMMAs do not reach the tensor pipe's rate).
 //
@@ -15,20 +15,20 @@
 // dP^T; dV, dK and dQ^T -- two issuing threads keep the tensor pipe fed while either
 // one waits on a barrier), 4..11 element-wise (warp w: tensor-memory lane quarter
 // w % 4, query half (w - 4) / 4; one key row per thread), 12..15 dQ drain (warp w:
-// lane quarter w % 4, i.e. 32 values of d; each takes all 128 columns of dQ^T out of
-// tensor memory at once, frees the columns, then issues the reductions while the next
-// step runs).  L2 absorbs fp32 reductions at about 20 bytes per clock per SM, so the
+// lane quarter w % 4, i.e. 32 values of d; each takes its columns of dQ^T out of
+// tensor memory at once, frees them, then issues the reductions while the next step
+// runs).  L2 absorbs fp32 reductions at about 20 bytes per clock per SM, so the
 // 64 KiB of dQ per step are drained off the element-wise warps' path.  Registers move
 // from the producer/UMMA warpgroup to the others with setmaxnreg: 72 + 3 x 144 <= 4 x 128.
-#include "bwd128_steps.cuh"
+#include "bwd_steps.cuh"
 #include "internal.h"
 
 namespace fa {
 namespace {
 
-using namespace b128;
+using namespace bsteps;
 
-// Barriers of this kernel beyond the per-step ones (bwd128_steps.cuh).
+// Barriers of this kernel beyond the per-step ones (bwd_steps.cuh).
 enum : int { B_KV = 0, B_FINAL = 17, B_ADONE = 18, NBAR = 20 };
 constexpr int OFF_MISC = NBAR * 8;  // tensor-memory base, abort flag
 constexpr int NTHREADS = 512;
@@ -36,16 +36,17 @@ static_assert(OFF_MISC + 8 <= OFF_LD, "small region");
 
 enum : int { SITE_PRODUCER = 0x211, SITE_MMA = 0x212, SITE_COMPUTE = 0x213, SITE_LAYOUT = 0x215 };
 
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(NTHREADS, 1)
-    bwd_d128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    bwd_tile_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const float* __restrict__ Lg, const float* __restrict__ Dg, float* __restrict__ dQacc,
                     __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV, int Nq, int Nk, int window,
                     float c_log2, float scale, int* status, unsigned long long* tile_counter, int head_group) {
+  using LY = Lay<D, 1>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* tiles = align1024(smem_raw + SMALL);
-  if (tiles + TILES > smem_raw + SMEM) {
+  if (tiles + LY::TILES > smem_raw + LY::SMEM) {
     // the dynamic shared memory base is too badly aligned for this layout: report, do nothing
     if (threadIdx.x == 0) atomicCAS(status, 0, SITE_LAYOUT);
     return;
@@ -112,15 +113,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (warp == 0 && !skip) {
     // ---------------------------------------------------------------- producer (whole warp)
     if (lane == 0) {
-      mbar_expect_tx(bar(B_KV), 2 * TILE);
-      for (int c = 0; c < 2; ++c) {
-        tma_load_3d(x.tb + T_K + c * 128 * 128, &tmK, bar(B_KV), c * 64, kt * BN, bh);
-        tma_load_3d(x.tb + T_V + c * 128 * 128, &tmV, bar(B_KV), c * 64, kt * BN, bh);
-      }
+      mbar_expect_tx(bar(B_KV), LY::KVB);
+      for (int c = 0; c < 2; ++c)  // at d = 64 the second K chunk is a copy of the first
+        tma_load_3d(LY::k(x.tb, 0) + c * CHUNK, &tmK, bar(B_KV), D == 128 ? c * 64 : 0, kt * BN, bh);
+      for (int c = 0; c < LY::TQ / CHUNK; ++c)
+        tma_load_3d(LY::v(x.tb, 0) + c * CHUNK, &tmV, bar(B_KV), c * 64, kt * BN, bh);
     }
     int last = -1;
     for (int it = 0; it < n_it; ++it) {
-      if (!produce_step(x, &tmQ, &tmdO, Lg, Dg, row0, Nq, (i0 + it) * BM, bh, it, lane, SITE_PRODUCER)) break;
+      if (!produce_step<LY>(x, &tmQ, &tmdO, Lg, Dg, row0, Nq, (i0 + it) * BM, bh, it, lane, SITE_PRODUCER)) break;
       last = it;
     }
     if (lane == 0 && *abort_flag) {
@@ -130,23 +131,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == 1 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- UMMA issuer A: S^T, dP^T
     bool ok = mbar_wait(bar(B_KV), 0, x.guard, SITE_MMA);
-    for (int it = 0; ok && it < n_it; ++it) ok = issue_s_dp(x, it, SITE_MMA);
+    for (int it = 0; ok && it < n_it; ++it) ok = issue_s_dp<LY>(x, it, 0, SITE_MMA);
     mma_commit(bar(B_ADONE));  // drain point for teardown
     if (ok && tile_counter != nullptr) atomicAdd(tile_counter, static_cast<unsigned long long>(n_it));
   } else if (warp == 2 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- UMMA issuer B: dV, dK, dQ^T
     for (int it = 0; it < n_it; ++it)
-      if (!issue_dv_dk_dq(x, it, it == 0, SITE_MMA)) break;
+      if (!issue_dv_dk_dq<LY>(x, it, 0, it == 0, SITE_MMA)) break;
     mma_commit(bar(B_FINAL));
   }
   } else if (warp >= 12) {
     regs_inc<144>();
     if (!skip) {
     // ---------------------------------------------------------------- dQ drain
+    pdl_wait();  // the workspace is cleared by the kernel before this one
     const int qw = warp & 3;
     for (int j = 0; j < n_it; ++j) {
       const int q0 = (i0 + j) * BM;
-      if (!drain_step(x, j, dQacc + (row0 + q0) * D + qw * 32 + lane, min(BM, Nq - q0), qw, SITE_COMPUTE)) break;
+      if (!drain_step<D>(x, j, dQacc + (row0 + q0) * D, min(BM, Nq - q0), qw, lane, SITE_COMPUTE)) break;
     }
     }
   } else {
@@ -158,14 +160,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int key = kt * BN + qw * 32 + lane;
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it)
-      ok = ew_step<CAUSAL>(x, it, kt, i0 + it, Nk, off, window, c_log2, qw, h, lane, SITE_COMPUTE);
-    // dK (times scale) and dV: this warp's lane quarter, d columns 64h .. 64h+63
+      ok = ew_step<LY, CAUSAL>(x, it, kt, i0 + it, Nk, off, window, c_log2, qw, h, lane, SITE_COMPUTE);
+    // dK (times scale) and dV: this warp's lane quarter, d columns (D/2) h .. (D/2) h + D/2 - 1
     if (ok) ok = mbar_wait_warp(bar(B_FINAL), 0, x.guard, SITE_COMPUTE);
     if (ok) {
       tc_fence_after();
-      uint32_t outp[64];
-      ew_load_dk_dv(x, qw, h, scale, n_it == 0, outp);
-      if (key < Nk) ew_store_dk_dv(outp, dK, dV, krow0 + key, h);
+      uint32_t outp[D / 2];
+      ew_load_dk_dv<D>(x, qw, h, scale, n_it == 0, outp);
+      if (key < Nk) ew_store_dk_dv<D>(outp, dK, dV, krow0 + key, h);
     }
     }
   }
@@ -185,25 +187,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 fa_status launch_t(const BwdLaunch& a) {
+  using LY = Lay<D, 1>;
   CUtensorMap mQ, mK, mV, mdO;
   if (!encode_bf16_3d(&mQ, a.Q, D, a.Nq, a.BH, 64, BM) || !encode_bf16_3d(&mdO, a.dO, D, a.Nq, a.BH, 64, BM) ||
       !encode_bf16_3d(&mK, a.K, D, a.Nk, a.BH, 64, BN) || !encode_bf16_3d(&mV, a.V, D, a.Nk, a.BH, 64, BN))
     return FA_ERR_CUDA;
-  auto kern = bwd_d128_kernel<CAUSAL>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM) != cudaSuccess)
+  auto kern = bwd_tile_kernel<D, CAUSAL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, LY::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
   const dim3 grid((a.Nk + BN - 1) / BN, a.BH);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  kern<<<grid, NTHREADS, SMEM, a.stream>>>(mQ, mK, mV, mdO, a.L, a.D, a.dQacc, static_cast<__nv_bfloat16*>(a.dK),
-                                           static_cast<__nv_bfloat16*>(a.dV), a.Nq, a.Nk, a.window, c_log2, a.scale,
-                                           a.status, a.counter, head_group(a.BH, a.Nq, a.Nk, D));
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  // Launched so that it may start while the workspace is being cleared: only the dQ
+  // drain touches the workspace, and it waits for the clearing kernel's end first;
+  // everything else it reads was complete before that kernel started.
+  const cudaError_t e = launch_pdl(kern, grid, dim3(NTHREADS), LY::SMEM, a.stream, mQ, mK, mV, mdO, a.L, a.D,
+                                   a.dQacc, static_cast<__nv_bfloat16*>(a.dK), static_cast<__nv_bfloat16*>(a.dV),
+                                   a.Nq, a.Nk, a.window, c_log2, a.scale, a.status, a.counter,
+                                   head_group(a.BH, a.Nq, a.Nk, D));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace
 
-fa_status launch_bwd_d128(const BwdLaunch& a) { return a.causal ? launch_t<true>(a) : launch_t<false>(a); }
+fa_status launch_bwd_tile(const BwdLaunch& a) {
+  if (a.d == 64) return a.causal ? launch_t<64, true>(a) : launch_t<64, false>(a);
+  return a.causal ? launch_t<128, true>(a) : launch_t<128, false>(a);
+}
 
 }  // namespace fa

@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- producer
+    pdl_wait();  // Q, K, V (and the O, L rows written below) belong to earlier kernels
     mbar_expect_tx(bar(C::B_Q), C::TILE);
     for (int c = 0; c < C::NCH; ++c)
       tma_load_3d(sb + C::OFF_Q + c * C::BM * C::SWB, &tmQ, bar(C::B_Q), c * C::CE, qt * C::BM, bh);
@@ -247,9 +248,10 @@ fa_status launch_fwd_t(const FwdLaunch& a) {
     return FA_ERR_CUDA;
   const dim3 grid((a.Nq + C::BM - 1) / C::BM, a.BH);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  kern<<<grid, 256, C::SMEM, a.stream>>>(mQ, mK, mV, static_cast<__nv_bfloat16*>(a.O), a.L, a.Nq, a.Nk, a.window,
-                                         c_log2, a.status, a.counter, head_group(a.BH, a.Nq, a.Nk, D));
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(kern, grid, dim3(256), C::SMEM, a.stream, mQ, mK, mV,
+                                   static_cast<__nv_bfloat16*>(a.O), a.L, a.Nq, a.Nk, a.window, c_log2, a.status,
+                                   a.counter, head_group(a.BH, a.Nq, a.Nk, D));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace

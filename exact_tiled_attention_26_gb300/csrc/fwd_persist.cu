@@ -31,11 +31,12 @@
 
 namespace fa {
 
-// Work counters of the persistent launches: one per launch, taken in turn and
-// zeroed on the launch's stream, so launches that overlap on different streams
-// never share one (up to kQueueSlots of them in flight at once).
+// Work counters of the persistent launches: one pair per launch, taken in turn,
+// each left zeroed by the launch that used it (queue_release), so launches that
+// overlap on different streams never share one (up to kQueueSlots of them in
+// flight at once).
 constexpr int kQueueSlots = 1024;
-__device__ unsigned int g_fwd_queue[kQueueSlots];
+__device__ unsigned int g_fwd_queue[2 * kQueueSlots];
 
 namespace {
 
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(PCfg<D>::NTHREADS, 1)
   regs_dec<56>();
   if (warp == 0 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- producer
+    pdl_wait();  // Q, K, V (and the O, L rows written below) belong to earlier kernels
     int kv = 0, jk = -1, jv = -1, kq = -1;  // K/V tiles issued; last K, V, Q load issued
     for (int k = 0;; ++k) {
       const int slot = k & 1;
@@ -366,6 +368,7 @@ __global__ void __launch_bounds__(PCfg<D>::NTHREADS, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TM_COLS);
   }
+  if (threadIdx.x == 0) queue_release(queue);
 }
 
 std::mutex g_q_mu;
@@ -388,7 +391,7 @@ fa_status launch_persist_t(const FwdLaunch& a) {
       g_q_base[dev] = static_cast<unsigned int*>(p);
       if (cudaDeviceGetAttribute(&g_nsm[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FA_ERR_CUDA;
     }
-    counter = g_q_base[dev] + g_q_next;
+    counter = g_q_base[dev] + 2 * g_q_next;
     g_q_next = (g_q_next + 1) % kQueueSlots;
     nsm = g_nsm[dev];
   }
@@ -399,14 +402,13 @@ fa_status launch_persist_t(const FwdLaunch& a) {
   auto kern = fwd_persist_kernel<D, MASK>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return FA_ERR_CUDA;
-  if (cudaMemsetAsync(counter, 0, sizeof(unsigned int), a.stream) != cudaSuccess) return FA_ERR_CUDA;
   const long long units = static_cast<long long>((a.Nq + C::BM - 1) / C::BM) * a.BH;
   const int grid = static_cast<int>(units < nsm ? units : nsm);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  kern<<<grid, C::NTHREADS, C::SMEM, a.stream>>>(mQ, mK, mV, static_cast<__nv_bfloat16*>(a.O), a.L, a.BH, a.Nq, a.Nk,
-                                         a.window, c_log2, head_group(a.BH, a.Nq, a.Nk, D), counter, a.status,
-                                         a.counter);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(kern, dim3(grid), dim3(C::NTHREADS), C::SMEM, a.stream, mQ, mK, mV,
+                                   static_cast<__nv_bfloat16*>(a.O), a.L, a.BH, a.Nq, a.Nk, a.window, c_log2,
+                                   head_group(a.BH, a.Nq, a.Nk, D), counter, a.status, a.counter);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace

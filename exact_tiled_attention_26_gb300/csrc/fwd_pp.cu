@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(PP::NTHREADS, 1)
     regs_dec<56>();
     if (warp == 0 && lane == 0 && !skip) {
       // ---------------------------------------------------------------- producer
+      pdl_wait();  // Q, K, V (and the O, L rows written below) belong to earlier kernels
       for (int t = 0; t < (hasB ? 2 : 1); ++t) {
         mbar_expect_tx(bar(C::B_Q + t), C::TILE);
         for (int c = 0; c < 2; ++c)
@@ -265,10 +266,10 @@ fa_status launch_pp_t(const FwdLaunch& a) {
   const int T = (a.Nq + C::BM - 1) / C::BM;
   const dim3 grid((T + 1) / 2, a.BH);
   const float c_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  kern<<<grid, C::NTHREADS, C::SMEM, a.stream>>>(mQ, mK, mV, static_cast<__nv_bfloat16*>(a.O), a.L, a.Nq, a.Nk,
-                                                 a.window, c_log2, a.status, a.counter,
-                                                 head_group(a.BH, a.Nq, a.Nk, C::D));
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(kern, grid, dim3(C::NTHREADS), C::SMEM, a.stream, mQ, mK, mV,
+                                   static_cast<__nv_bfloat16*>(a.O), a.L, a.Nq, a.Nk, a.window, c_log2, a.status,
+                                   a.counter, head_group(a.BH, a.Nq, a.Nk, C::D));
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // namespace

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include <utility>
+
 #include "../../include/fa.h"
 
 namespace fa {
@@ -52,6 +54,26 @@ __host__ __device__ inline void query_tile_range(int kt, int Br, int Bc, int Nq,
   }
   *lo = l;
   *hi = h;
+}
+
+// Launch a kernel that may start before the previous kernel on the stream has
+// ended (programmatic dependent launch): the kernel must call pdl_wait (ptx.cuh)
+// before it touches anything that kernel writes, and everything it does before
+// that must be safe to overlap with it.  It overlaps only if the kernel before it
+// calls pdl_trigger (otherwise it starts when that kernel ends).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // Shape and mask checks of the general-mask entry points (fa_fwd_ex's rules);
@@ -123,15 +145,20 @@ struct BwdLaunch {
   int* status;
   unsigned long long* counter;
 };
+// One-kernel backward, one CTA per key tile: d = 32 (bwd.cu), d = 64 and 128 (bwd_tile.cu).
 fa_status launch_bwd(const BwdLaunch& a);
-fa_status launch_bwd_d128(const BwdLaunch& a);
+fa_status launch_bwd_tile(const BwdLaunch& a);
+// One-kernel backward, d = 64 and 128, one CTA per SM taking key tiles from a queue
+// (bwd_persist.cu).
+fa_status launch_bwd_persist(const BwdLaunch& a);
 // Two-kernel backward (d = 64 or 128): dK, dV by key tile, then dQ by query tile,
 // written directly to dQ (bf16); needs no workspace.
-// d = 128 one-kernel backward, one CTA per SM taking key tiles from a queue (bwd128p.cu).
-fa_status launch_bwd_d128_persist(const BwdLaunch& a);
 fa_status launch_bwd_two_kernel(const BwdLaunch& a, void* dQ);
 
 fa_status launch_preprocess(const void* O, const void* dO, float* D, long long rows, int d, cudaStream_t s);
+// Zero `bytes` (a multiple of 16) at 16-byte aligned `p`: an ordinary launch, so that a
+// kernel launched after it with launch_pdl starts only once everything before it ended.
+fa_status launch_zero(void* p, size_t bytes, cudaStream_t s);
 fa_status launch_dq_convert(const float* dQacc, void* dQ, long long n, float scale, cudaStream_t s);
 fa_status launch_timeout_probe(int limit_us, cudaStream_t s, int* status);
 fa_status launch_selftest(int mode, const void* A, const void* B, float* C, int K, int N, cudaStream_t s,

@@ -345,6 +345,32 @@ FA_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Programmatic dependent launch (a kernel launched with launch_pdl, internal.h, may
+// start while the kernel before it on the stream is still running).  pdl_wait:
+// block until that kernel has completed and its memory writes are visible (a no-op
+// when the launch was an ordinary one).  pdl_trigger: let the next kernel on the
+// stream, if launched with launch_pdl, start now (its own pdl_wait still orders
+// its reads after this kernel's end).  Only the workspace clear triggers early: its
+// dependent, the backward kernel, has loads and products to do before it waits.
+// A dependent that could only wait (the dQ convert, the preprocess, the forward)
+// would hold SMs that another stream's kernels could use, so kernels followed by
+// one of those never trigger: their dependents start when they end.
+FA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+FA_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// End of a persistent launch, one thread per CTA after the CTA's last unit fetch:
+// q[0] counts the units taken, q[1] the CTAs finished.  The last CTA to finish
+// zeroes both, so the slot is ready for the next launch that takes it (every
+// launch starts from zeroes, and a launch that never ran left them untouched).
+FA_DEV void queue_release(unsigned int* q) {
+  __threadfence();
+  if (atomicAdd(q + 1, 1u) == gridDim.x * gridDim.y * gridDim.z - 1) {
+    q[0] = 0u;
+    q[1] = 0u;
+    __threadfence();
+  }
+}
+
 // Round a dynamic shared-memory pointer up so that its shared-window address is
 // 1024-byte aligned (swizzled operand tiles need it).
 FA_DEV uint8_t* align1024(uint8_t* p) {

@@ -266,10 +266,11 @@ fa_status fa_debug_set_tile_counter(unsigned long long* dev_counter);
  *   2: two kernels, key/value tiles outer for dK and dV, then query tiles outer
  *      for dQ (S and P recomputed in both); no workspace, no reductions;
  *   3: form 1 with one CTA per SM taking key tiles from a queue, consecutive
- *      tiles overlapped (d = 128; other d run form 1 in its place; the same
- *      1024 work counters rule as fa_debug_set_fwd_form's form 3);
- *   0: the library's default, chosen by measurement on GB300: form 2 at d = 64,
- *      form 3 at d = 128.
+ *      tiles overlapped (d = 64 and 128; the same 1024 work counters rule as
+ *      fa_debug_set_fwd_form's form 3);
+ *   0: the library's default, chosen by measurement on GB300: form 3 at
+ *      d = 128; at d = 64 form 3 when B*H times the visible 128 x 128 tile
+ *      pairs per head (fa_tile_pairs_ex) exceeds 3072, else form 2.
  * d = 32 always runs form 1.  Process-wide setting; FA_ERR_INVALID_ARG for
  * other values.
  */
@@ -283,8 +284,9 @@ fa_status fa_debug_set_bwd_split(int split);
  *   2: two query tiles per CTA whose softmax and tensor-core work take turns;
  *   3: one CTA per SM taking query tiles from a queue, consecutive tiles
  *      overlapped (any d).  Each launch takes the next of 1024 work counters in
- *      a static device array (no allocation) and zeroes it on its stream; at
- *      most 1024 such launches may be in flight at once across streams;
+ *      a static device array (no allocation), which its last CTA leaves zeroed
+ *      for the counter's next launch; at most 1024 such launches may be in
+ *      flight at once across streams;
  *   0: the library's default, chosen by measurement on GB300: form 3 for d <= 64,
  *      and for d = 128 when no query tile sees more than 128 key tiles; else 1.
  * Process-wide setting; FA_ERR_INVALID_ARG for other values.
@@ -318,7 +320,8 @@ fa_status fa_debug_set_kernel_events(int which, void* start, void* stop);
  * the current settings (the numbers of fa_debug_set_fwd_form and
  * fa_debug_set_bwd_split).  Host only; the argument checks of fa_fwd_ex.
  */
-fa_status fa_selected_forms(int Nq, int Nk, int d, int causal, int window, int* fwd_form, int* bwd_form);
+fa_status fa_selected_forms(int B, int H, int Nq, int Nk, int d, int causal, int window, int* fwd_form,
+                            int* bwd_form);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of the

@@ -122,6 +122,12 @@ def test_backward_split_selection(fa_lib):
     try:
         assert fa.fa_debug_set_bwd_split(4) == fa.FA_ERR_INVALID_ARG
         assert fa.fa_debug_set_bwd_split(-1) == fa.FA_ERR_INVALID_ARG
+        assert fa.fa_debug_set_bwd_split(0) == fa.FA_OK
+        # d = 64 default: persistent above 3072 visible tile pairs, else two kernels
+        assert fa.fa_bwd_workspace_size(2, 16, 4096, 64, 1) == 2 * 16 * 4096 * 64 * 4  # 16896 pairs
+        assert fa.fa_bwd_workspace_size(4, 8, 1024, 64, 1) == 0  # 1152 pairs
+        assert fa.fa_bwd_workspace_size(4, 8, 1024, 64, 0) == 0  # 2048 pairs
+        assert fa.fa_bwd_workspace_size(4, 8, 2048, 64, 1) == 4 * 8 * 2048 * 64 * 4  # 4352 pairs
         assert fa.fa_debug_set_bwd_split(2) == fa.FA_OK
         assert fa.fa_bwd_workspace_size(2, 16, 4096, 128, 1) == 0
         assert fa.fa_bwd_workspace_size(2, 16, 4096, 64, 1) == 0
@@ -177,19 +183,23 @@ def test_forward_form_switch(fa_lib):
     assert fa.fa_debug_set_fwd_form(-1) == fa.FA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("Nq,Nk,d,causal,window,fwd,bwd", [
-    (32768, 32768, 128, 1, 0, 1, 3),   # 256 key tiles per query tile: the one-tile forward
-    (32768, 32768, 128, 0, 0, 1, 3),
-    (16384, 16384, 128, 1, 0, 3, 3),   # up to 128: persistent
-    (8192, 8192, 128, 1, 0, 3, 3),
-    (4096, 4096, 128, 0, 0, 3, 3),
-    (8192, 8192, 128, 1, 1024, 3, 3),  # a window: few tiles per row
-    (2048, 32768, 128, 1, 0, 1, 3),    # prefill: long rows; the backward is persistent at d = 128
-    (1024, 1024, 64, 1, 0, 3, 2),      # d = 64: persistent forward, two-kernel backward
-    (256, 256, 32, 0, 0, 3, 1),        # d = 32: persistent forward, one-kernel backward
+@pytest.mark.parametrize("BH,Nq,Nk,d,causal,window,fwd,bwd", [
+    (32, 32768, 32768, 128, 1, 0, 1, 3),   # 256 key tiles per query tile: the one-tile forward
+    (32, 32768, 32768, 128, 0, 0, 1, 3),
+    (32, 16384, 16384, 128, 1, 0, 3, 3),   # up to 128: persistent
+    (32, 8192, 8192, 128, 1, 0, 3, 3),
+    (1, 4096, 4096, 128, 0, 0, 3, 3),
+    (32, 8192, 8192, 128, 1, 1024, 3, 3),  # a window: few tiles per row
+    (32, 2048, 32768, 128, 1, 0, 1, 3),    # prefill: long rows; the backward is persistent at d = 128
+    (32, 1024, 1024, 64, 1, 0, 3, 2),      # d = 64, 1152 tile pairs: two-kernel backward
+    (128, 1024, 1024, 64, 1, 0, 3, 3),     # 4608 pairs: persistent backward
+    (32, 8192, 8192, 64, 1, 0, 3, 3),
+    (1, 8192, 8192, 64, 1, 0, 3, 2),       # one head, 2080 pairs
+    (32, 256, 256, 32, 0, 0, 3, 1),        # d = 32: persistent forward, one-kernel backward
 ])
-def test_selected_forms(fa_lib, Nq, Nk, d, causal, window, fwd, bwd):
-    assert fa_lib.fa_selected_forms(Nq, Nk, d, causal, window) == (fa_lib.FA_OK, fwd, bwd)
+def test_selected_forms(fa_lib, BH, Nq, Nk, d, causal, window, fwd, bwd):
+    assert fa_lib.fa_selected_forms(1, BH, Nq, Nk, d, causal, window) == (fa_lib.FA_OK, fwd, bwd)
+    assert fa_lib.fa_selected_forms(BH, 1, Nq, Nk, d, causal, window) == (fa_lib.FA_OK, fwd, bwd)
 
 
 def test_selected_forms_follow_overrides(fa_lib):
@@ -197,14 +207,19 @@ def test_selected_forms_follow_overrides(fa_lib):
     try:
         fa.check(fa.fa_debug_set_fwd_form(1))
         fa.check(fa.fa_debug_set_bwd_split(2))
-        assert fa.fa_selected_forms(4096, 4096, 128, 1, 0) == (fa.FA_OK, 1, 2)
+        assert fa.fa_selected_forms(2, 16, 4096, 4096, 128, 1, 0) == (fa.FA_OK, 1, 2)
+        assert fa.fa_selected_forms(2, 16, 4096, 4096, 64, 1, 0) == (fa.FA_OK, 1, 2)
         fa.check(fa.fa_debug_set_fwd_form(2))
-        assert fa.fa_selected_forms(4096, 4096, 64, 1, 0)[1] == 1  # two query tiles per CTA exists at d = 128 only
+        assert fa.fa_selected_forms(2, 16, 4096, 4096, 64, 1, 0)[1] == 1  # two query tiles per CTA exists at d = 128 only
+        fa.check(fa.fa_debug_set_bwd_split(3))
+        assert fa.fa_selected_forms(1, 1, 1024, 1024, 64, 1, 0)[2] == 3
+        assert fa.fa_selected_forms(1, 1, 1024, 1024, 32, 1, 0)[2] == 1  # d = 32: one kernel only
     finally:
         fa.fa_debug_set_fwd_form(0)
         fa.fa_debug_set_bwd_split(0)
-    assert fa.fa_selected_forms(100, 100, 48, 1, 0)[0] == fa.FA_ERR_UNSUPPORTED
-    assert fa.fa_selected_forms(100, 100, 64, 0, 8)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_selected_forms(1, 1, 100, 100, 48, 1, 0)[0] == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_selected_forms(1, 1, 100, 100, 64, 0, 8)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_selected_forms(-1, 1, 100, 100, 64, 0, 0)[0] == fa.FA_ERR_INVALID_ARG
 
 
 def test_bwd_plan_is_one_reading_under_a_flipping_setting(fa_lib):

@@ -1,7 +1,7 @@
 """GPU parity of the forms of the d = 64 and d = 128 backward ("CS336 Assignment 2
 notes" §1.4): form 1 (one kernel over key tiles, dQ reduced in an fp32 workspace),
 form 2 (a key-tile kernel for dK, dV and a query-tile kernel for dQ) and form 3
-(form 1 with one CTA per SM taking key tiles from a queue; d = 128), each against
+(form 1 with one CTA per SM taking key tiles from a queue), each against
 the float64 oracle, whichever of them is the library's default."""
 import numpy as np
 import pytest
@@ -93,12 +93,13 @@ def test_small_workload_form2_d64(causal):
     assert got["tiles"][1] == 32 * lib().fa_tile_pairs(1024, 64, causal, 1)
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("B,H,N,causal,window", [(2, 3, 1000, True, 0), (1, 5, 700, False, 0), (3, 2, 777, True, 100),
                                                  (4, 40, 256, True, 0), (2, 16, 4096, True, 0)])
-def test_persistent_form_equals_form1(B, H, N, causal, window):
+def test_persistent_form_equals_form1(B, H, N, causal, window, d):
     """Form 3 runs each key tile exactly as form 1 does: dK and dV agree bit for bit;
     dQ is summed in fp32 reductions whose order varies."""
-    Q, K, V, dO = si.make_qkvdo(B, H, N, 128, seed=2200 + N + window)
+    Q, K, V, dO = si.make_qkvdo(B, H, N, d, seed=2200 + N + window)
     a = run_gpu(Q, K, V, dO, causal, counter=True, split=1, window=window)
     b = run_gpu(Q, K, V, dO, causal, counter=True, split=3, window=window)
     assert torch.equal(a["dK"], b["dK"]) and torch.equal(a["dV"], b["dV"])
