@@ -186,6 +186,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // K and V of this unit into buffer k % NKV, once the last readers of unit k - NKV
       // (which used it) are done
       const int b = k % NKV;
+      if (lane == 0 && k >= NKV) {  // used once per unit: bring the descriptors back into their cache
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+      }
       if (k >= NKV && !mbar_wait_warp(bar(kvfree(b)), (k / NKV - 1) & 1, x.guard, SITE_P_PRODUCER)) break;
       if (lane == 0) {
         mbar_expect_tx(bar(kvfull(b)), LY::KVB);
