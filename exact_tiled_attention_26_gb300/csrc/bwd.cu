@@ -1,6 +1,5 @@
 // Backward pass of exact tiled attention on sm_103a: main kernel for head size 32
-// (head sizes 64 and 128 run the pipelined kernels of bwd_tile.cu and bwd_persist.cu;
-// the d = 128 branches below are this first version's and are not instantiated).
+// (head sizes 64 and 128 run the pipelined kernels of bwd_tile.cu and bwd_persist.cu).
 //
 // "CS336 Assignment 2 notes" §1.4, Equations 13-19, with the key/value tiles
 // in the outer loop (kernel 1 of the notes' two-kernel scheme).  One CTA owns
@@ -19,10 +18,7 @@
 //           memory and added into an fp32 [B,H,N,d] workspace with one bulk
 //           reduce-add (performed in L2) per tile; a later pass rounds it.
 //
-// Tile shapes: 128 keys x Br queries, Br = 64 for d = 128 (tensor-memory
-// budget: dK 128 + dV 128 + S 64 + dP 64 + two dQ^T buffers of 64 = 512
-// columns) and 128 for d <= 64.  For d = 128 dQ is formed as dQ^T = K^T dS^T
-// (M = d = 128); for d <= 64 as dQ = dS K (M = Br = 128).
+// Tile shapes: 128 keys x 128 queries; dQ is formed as dQ = dS K (M = 128 queries).
 //
 // Warp roles: warp 0 TMA producer (K, V once; Q_i, dO_i 2-stage ring), warp 1
 // UMMA issuer (one thread), warps 4..7 element-wise work (one thread per key
@@ -38,9 +34,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdCfg {
-  static constexpr int BN = kBwdBc;              // keys per CTA (tensor-memory lanes)
-  static constexpr int BM = (D == 128) ? 64 : 128;  // queries per inner step
-  static constexpr bool DQT = (D == 128);        // dQ formed transposed
+  static_assert(D == 32, "head sizes 64 and 128 run bwd_tile.cu / bwd_persist.cu");
+  static constexpr int BN = kBwdBc;  // keys per CTA (tensor-memory lanes)
+  static constexpr int BM = 128;     // queries per inner step
   static constexpr int SWB = (D * 2 >= 128) ? 128 : D * 2;
   static constexpr int CE = SWB / 2, NCH = D / CE;
   static constexpr int KV_BYTES = BN * D * 2;
@@ -61,7 +57,7 @@ struct BwdCfg {
   static constexpr int SMEM_USED = OFF_MISC + 16;
   static constexpr int SMEM = (SMEM_USED + 1024 > 120 * 1024) ? SMEM_USED + 1024 : 120 * 1024;
   // tensor memory columns
-  static constexpr int DQC = DQT ? BM : D;  // columns of one dQ buffer
+  static constexpr int DQC = D;  // columns of one dQ buffer
   static constexpr int TM_DK = 0, TM_DV = D, TM_S = 2 * D, TM_DP = 2 * D + BM, TM_DQ = 2 * D + 2 * BM;
   static constexpr int TM_COLS = 512;
   static_assert(TM_DQ + 2 * DQC <= TM_COLS, "tensor memory budget");
@@ -157,8 +153,7 @@ __global__ void __launch_bounds__(256, 1)
     constexpr uint32_t idS = idesc_bf16(128, C::BM, false, false);  // K|V (K-major) x Q|dO (K-major)
     constexpr uint32_t idDV = idesc_bf16(128, D, false, true);      // P^T (tensor mem) x dO (N-major)
     constexpr uint32_t idDK = idesc_bf16(128, D, true, true);       // dS^T (M-major) x Q (N-major)
-    constexpr uint32_t idDQ = C::DQT ? idesc_bf16(128, C::BM, true, false)  // K^T (M-major) x dS (K-major)
-                                     : idesc_bf16(128, D, false, true);     // dS (K-major) x K (N-major)
+    constexpr uint32_t idDQ = idesc_bf16(128, D, false, true);      // dS (K-major) x K (N-major)
     bool ok = mbar_wait(bar(C::B_KV), 0, guard, SITE_BWD_MMA);
     for (int it = 0; ok && it < n_it; ++it) {
       const int s = it & 1;
@@ -194,17 +189,10 @@ __global__ void __launch_bounds__(256, 1)
                idDK, (it > 0 || ks > 0));
       // dQ_i (this key tile's part)
       const uint32_t dq = tmem + C::TM_DQ + s * C::DQC;
-      if constexpr (C::DQT) {
 #pragma unroll
-        for (int ks = 0; ks < C::BN / 16; ++ks)
-          mma_ss(dq, sdesc_mnmajor<C::SWB, C::BN>(sb + C::OFF_K, ks), sdesc_kmajor<128, C::BM>(sb + C::OFF_DS, ks),
-                 idDQ, ks > 0);
-      } else {
-#pragma unroll
-        for (int ks = 0; ks < C::BN / 16; ++ks)
-          mma_ss(dq, sdesc_kmajor<128, C::BM>(sb + C::OFF_DS, ks), sdesc_mnmajor<C::SWB, C::BN>(sb + C::OFF_K, ks),
-                 idDQ, ks > 0);
-      }
+      for (int ks = 0; ks < C::BN / 16; ++ks)
+        mma_ss(dq, sdesc_kmajor<128, C::BM>(sb + C::OFF_DS, ks), sdesc_mnmajor<C::SWB, C::BN>(sb + C::OFF_K, ks),
+               idDQ, ks > 0);
       mma_commit(bar(C::B_DQFULL + s));
       mma_commit(bar(C::B_QEMPTY + s));
     }
@@ -280,29 +268,17 @@ __global__ void __launch_bounds__(256, 1)
       if (ct == 0) bulk_wait_read0();  // the previous tile's add has read dQs
       named_bar_sync(1, 128);
       const uint32_t dq = tl + C::TM_DQ + s * C::DQC;
-      if constexpr (C::DQT) {
-        // lane = d index, columns = queries
+      // lane = query row, columns = d
 #pragma unroll
-        for (int c = 0; c < C::BM / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(dq + 32 * c, r);
-          tmem_ld_wait<32>(r);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(dq + 32 * c, r);
+        tmem_ld_wait<32>(r);
+        float4* rowp = reinterpret_cast<float4*>(dQs + kr * D + 32 * c);
 #pragma unroll
-          for (int x = 0; x < 32; ++x) dQs[(32 * c + x) * D + kr] = __uint_as_float(r[x]);
-        }
-      } else {
-        // lane = query row, columns = d
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(dq + 32 * c, r);
-          tmem_ld_wait<32>(r);
-          float4* rowp = reinterpret_cast<float4*>(dQs + kr * D + 32 * c);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            rowp[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-        }
+        for (int v = 0; v < 8; ++v)
+          rowp[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
       }
       tc_fence_before();
       mbar_arrive(bar(C::B_DQFREE + s));

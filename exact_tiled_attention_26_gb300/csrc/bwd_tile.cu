@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mma_commit(bar(B_FINAL));
   }
   } else if (warp >= 12) {
-    regs_inc<144>();
+    regs_inc<D == 64 ? 136 : 144>();
     if (!skip) {
     // ---------------------------------------------------------------- dQ drain
     pdl_wait();  // the workspace is cleared by the kernel before this one
@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     }
   } else {
-    regs_inc<144>();
+    regs_inc<D == 64 ? 152 : 144>();  // 72 + 152 x 2 + 136 = 4 x 128 at d = 64
     if (!skip) {
     // ---------------------------------------------------------------- element-wise warps
     const int qw = warp & 3;        // tensor-memory lane quarter

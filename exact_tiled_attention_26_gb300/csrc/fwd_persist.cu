@@ -22,7 +22,7 @@
 // next unit; warps 8..11 wait for the unit's last P V product, take O out of
 // tensor memory, release it to the next unit's first product and store O and L.
 // Registers move with setmaxnreg: 56 (TMA, UMMA issue) + 232 (softmax) + 216
-// (epilogue) = 3 x 168.
+// (epilogue) = 3 x 168 at d = 128; 64 + 232 + 208 below.
 #include <mutex>
 
 #include "fwd_softmax.cuh"
@@ -59,6 +59,11 @@ struct PCfg {
                        B_EFREE = 31,   // [unit parity] read by the epilogue warps
                        NBAR = 33;
   static constexpr int NTHREADS = 384;
+  // setmaxnreg shares of the launch's 3 x 168 registers per thread: TMA and UMMA issue,
+  // softmax (232), epilogue.  At d <= 64 the issuing code needs a little more than 56
+  // and the epilogue holds a narrower O.
+  static constexpr int REG_ISSUE = D == 128 ? 56 : 64, REG_EPI = D == 128 ? 216 : 208;
+  static_assert(REG_ISSUE + 232 + REG_EPI == 3 * 168, "register split");
   static constexpr int UEMPTY_COUNT = 1 + 1 + 4 + 4;  // S issuer, P V issuer, 4 softmax and 4 epilogue warps
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tensor-memory base, abort flag, unit ring
   static constexpr int OFF_ROWS = OFF_MISC + 16;       // [2][3][128] floats: m, l, l of the bf16 weights
@@ -154,7 +159,7 @@ __global__ void __launch_bounds__(PCfg<D>::NTHREADS, 1)
   float* rows = reinterpret_cast<float*>(smem + C::OFF_ROWS);
 
   if (warp < 4) {
-  regs_dec<56>();
+  regs_dec<PCfg<D>::REG_ISSUE>();
   if (warp == 0 && lane == 0 && !skip) {
     // ---------------------------------------------------------------- producer
     pdl_wait();  // Q, K, V (and the O, L rows written below) belong to earlier kernels
@@ -318,7 +323,7 @@ __global__ void __launch_bounds__(PCfg<D>::NTHREADS, 1)
     }
   }
   } else {
-  regs_inc<216>();  // from the launch's 168: an increase
+  regs_inc<PCfg<D>::REG_EPI>();  // from the launch's 168: an increase
   if (!skip) {
     // ---------------------------------------------------------------- epilogue
     const int wq = warp & 3;
