@@ -170,8 +170,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int k = 0;; ++k) {
       const int slot = k & 1;
       int u = 0;
-      if (lane == 0) {
-        u = static_cast<int>(atomicAdd(queue, 1u));
+      if (lane == 0) {  // the CTA's own first unit, then the queue after the grid's first units
+        u = k == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x + atomicAdd(queue, 1u));
         if (u >= U) u = -1;
       }
       u = __shfl_sync(0xffffffffu, u, 0);

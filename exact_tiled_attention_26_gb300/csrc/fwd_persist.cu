@@ -166,7 +166,9 @@ __global__ void __launch_bounds__(PCfg<D>::NTHREADS, 1)
     int kv = 0, jk = -1, jv = -1, kq = -1;  // K/V tiles issued; last K, V, Q load issued
     for (int k = 0;; ++k) {
       const int slot = k & 1;
-      int u = static_cast<int>(atomicAdd(queue, 1u));
+      // the first unit is the CTA's own (no queue round trip before the first loads),
+      // the rest come from the queue after the grid's first units
+      int u = k == 0 ? static_cast<int>(blockIdx.x) : static_cast<int>(gridDim.x + atomicAdd(queue, 1u));
       if (u >= U) u = -1;
       // slot k % 2 last held unit k-2: every consumer has read it
       if (k >= 2 && !mbar_wait(bar(C::B_UEMPTY + slot), ((k >> 1) & 1) ^ 1, guard, SITE_PF_PRODUCER)) break;

@@ -359,7 +359,7 @@ FA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 FA_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // End of a persistent launch, one thread per CTA after the CTA's last unit fetch:
-// q[0] counts the units taken, q[1] the CTAs finished.  The last CTA to finish
+// q[0] counts the units taken from the queue, q[1] the CTAs finished.  The last CTA to finish
 // zeroes both, so the slot is ready for the next launch that takes it (every
 // launch starts from zeroes, and a launch that never ran left them untouched).
 FA_DEV void queue_release(unsigned int* q) {
