@@ -243,6 +243,11 @@ FA_DEV bool drain_step(const Ctx& x, int g, float* tile, int nq, int qw, int lan
 template <class LY, bool CAUSAL>
 FA_DEV bool ew_step(const Ctx& x, int g, int kt, int qt, int Nk, int off, int window, float c_log2, int qw, int h,
                     int lane, int site) {
+  // d = 128: P^T goes to the dV product only after dP^T is out of tensor memory, so that
+  // the dV product (a TS UMMA, whose tensor-memory reads slow tcgen05.ld down) does not
+  // run under that load (measured +0.4-1.2% at d = 128; at d = 64, where dV is shorter
+  // and its early start matters more, releasing each half of P^T at once is 2% faster).
+  constexpr bool DP_FIRST = LY::TQ == 128 * 128 * 2;
   const int s = g & 1;
   const int kr = qw * 32 + lane;  // key row (tensor-memory lane)
   const int key = kt * BN + kr;
@@ -296,10 +301,13 @@ FA_DEV bool ew_step(const Ctx& x, int g, int kt, int qt, int Nk, int off, int wi
     };
     if (masked) body(std::true_type{}); else body(std::false_type{});
     tmem_st16(rs + 64 * h + 16 * c, pk + 16 * c);
-    tmem_st_wait();
-    tc_fence_before();
-    mbar_arrive(x.bar(B_PREADY + 2 * s + c));
+    if (!DP_FIRST) {
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(x.bar(B_PREADY + 2 * s + c));
+    }
   }
+  if (DP_FIRST) tmem_st_wait();
   // ---- dS^T = P^T (dP^T - D), from the same bf16 P that enters dV; two sub-chunks
   if (!mbar_wait_warp(x.bar(B_DPFULL), g & 1, x.guard, site)) return false;
   tc_fence_after();
@@ -311,6 +319,10 @@ FA_DEV bool ew_step(const Ctx& x, int g, int kt, int qt, int Nk, int off, int wi
   tmem_ld32(rd + 64 * h + 32, rdp + 32);
   tmem_ld_wait<64>(rdp);
   tc_fence_before();
+  if (DP_FIRST) {
+    mbar_arrive(x.bar(B_PREADY + 2 * s));
+    mbar_arrive(x.bar(B_PREADY + 2 * s + 1));
+  }
   mbar_arrive(x.bar(B_DPCONS));
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
