@@ -88,3 +88,52 @@ def test_other_forms_long_shape_equal_one_tile_form(form):
     o1, l1 = _fwd(1, Q, K, V, True, 0)
     o2, l2 = _fwd(form, Q, K, V, True, 0)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_work_counters_survive_reuse():
+    """The persistent kernels take their work counters from a fixed pool of 1024 per
+    pass, each launch leaving its counter zeroed for the pool's next round.  Run more
+    launches than the pool holds (forward and backward, on one stream, shapes whose
+    grids differ so that units are left for the queue), then check a launch of each
+    against the one-tile kernels: a counter left non-zero would skip units."""
+    fa = lib()
+    s = torch.cuda.current_stream().cuda_stream
+    B, H, N, d = 2, 16, 1280, 128  # 10 tiles x 32 heads = 320 units per pass: more than one per SM
+    Q, K, V, dO = si.make_qkvdo(B, H, N, d, seed=4711)
+    q, k, v, do = (t.cuda() for t in (Q, K, V, dO))
+    o, lse = torch.empty_like(q), torch.empty(B, H, N, dtype=torch.float32, device="cuda")
+    D = torch.empty_like(lse)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d, True), dtype=torch.uint8, device="cuda")
+    scale = 1 / math.sqrt(d)
+
+    def step():
+        fa.check(fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d, True,
+                           scale, s))
+        fa.check(fa.fa_bwd_preprocess(o.data_ptr(), do.data_ptr(), D.data_ptr(), B, H, N, d, s))
+        fa.check(fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                           D.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d, True, scale,
+                           ws.data_ptr(), ws.numel(), s))
+
+    fa.check(fa.fa_debug_set_fwd_form(3))
+    fa.check(fa.fa_debug_set_bwd_split(3))
+    try:
+        for _ in range(1100):  # every counter of both pools used at least once, some twice
+            step()
+        torch.cuda.synchronize()
+        got = [t.clone() for t in (o, lse, dk, dv)]
+    finally:
+        fa.fa_debug_set_fwd_form(0)
+        fa.fa_debug_set_bwd_split(0)
+    st, detail = fa.fa_poll_device_error(s)
+    fa.check(st, f"device status word (site {detail:#x})")
+    fa.check(fa.fa_debug_set_fwd_form(1))
+    fa.check(fa.fa_debug_set_bwd_split(1))
+    try:
+        step()
+        torch.cuda.synchronize()
+    finally:
+        fa.fa_debug_set_fwd_form(0)
+        fa.fa_debug_set_bwd_split(0)
+    for g, r in zip(got, (o, lse, dk, dv)):
+        assert torch.equal(g, r)
