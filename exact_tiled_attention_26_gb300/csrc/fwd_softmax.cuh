@@ -99,10 +99,12 @@ FA_DEV bool softmax_tile(SoftmaxRow& st, uint32_t tS, uint32_t tO, bool first, i
   // a row whose keys so far were all masked (a window's first tile) keeps
   // m = -inf; its P is 0 and the first visible tile rescales by 0
   const float neg_m = (WINDOW && st.m_run == -INFINITY) ? 0.f : -st.m_run;
-  // two columns per packed f32x2 instruction: exponent argument, running sums of
-  // P (for L) and of P as rounded to bf16 (for O's normaliser); two chains each
+  // two columns per packed f32x2 instruction: exponent argument and running sum of
+  // P (for L); the sum of P as rounded to bf16 (for O's normaliser) adds the packed
+  // bf16 pair itself, one mixed-precision add per column; two chains each
   const uint64_t cc2 = f2pack(c_log2, c_log2), nm2 = f2pack(neg_m, neg_m);
-  uint64_t ls[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)}, rs[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+  uint64_t ls[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+  float rl[2] = {0.f, 0.f}, rh[2] = {0.f, 0.f};
   uint32_t p[64];
 #pragma unroll
   for (int k = 0; k < 128; k += 2) {
@@ -112,11 +114,12 @@ FA_DEV bool softmax_tile(SoftmaxRow& st, uint32_t tS, uint32_t tO, bool first, i
     ls[(k >> 1) & 1] = fadd2(ls[(k >> 1) & 1], f2pack(p0, p1));
     const uint32_t pk = pack_bf16x2(p0, p1);
     p[k >> 1] = pk;
-    rs[(k >> 1) & 1] = fadd2(rs[(k >> 1) & 1], f2pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u)));
+    add_bf16x2_f32(pk, rl[(k >> 1) & 1], rh[(k >> 1) & 1]);
   }
   float a0, a1, a2, a3;
   f2unpack(fadd2(ls[0], ls[1]), a0, a1);
-  f2unpack(fadd2(rs[0], rs[1]), a2, a3);
+  a2 = rl[0] + rl[1];
+  a3 = rh[0] + rh[1];
   st.l_run += a0 + a1;
   st.lr_run += a2 + a3;
   tmem_st32(tS, p);

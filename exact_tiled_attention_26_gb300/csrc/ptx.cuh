@@ -345,6 +345,15 @@ FA_DEV uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// lo += the low bf16 of pk, hi += its high bf16: two mixed-precision adds (sm_100
+// and later), each widening its bf16 operand exactly and rounding the f32 sum to
+// nearest, so the same as adding the two halves unpacked to f32.
+FA_DEV void add_bf16x2_f32(uint32_t pk, float& lo, float& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n add.rn.f32.bf16 %0, l, %0;\n add.rn.f32.bf16 %1, h, %1;\n}"
+      : "+f"(lo), "+f"(hi)
+      : "r"(pk));
+}
+
 // Programmatic dependent launch (a kernel launched with launch_pdl, internal.h, may
 // start while the kernel before it on the stream is still running).  pdl_wait:
 // block until that kernel has completed and its memory writes are visible (a no-op
