@@ -275,9 +275,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int h = (warp - 4) >> 2;
     bool ok = true;
     int g = 0;
+    // dK, dV rows of the previous unit, held from its end until the next unit's K, V
+    // are in shared memory, so that their stores do not compete with that load
+    uint32_t outp[D / 2];
+    size_t prow0 = 0;
+    int pvalid = 0;
+    bool pending = false;
     for (int k = 0; ok; ++k) {
       int u = 0;
-      if (!(ok = take_unit(k, true, SITE_P_COMPUTE, &u)) || u < 0) break;
+      if (!(ok = take_unit(k, true, SITE_P_COMPUTE, &u))) break;
+      if (pending) {
+        if (u >= 0 && !(ok = mbar_wait_warp(bar(kvfull(k % NKV)), (k / NKV) & 1, x.guard, SITE_P_COMPUTE))) break;
+        ew_store_dk_dv<D>(outp, dK, dV, prow0, pvalid, h, lane);
+        pending = false;
+      }
+      if (u < 0) break;
       const BUnit w = decode(u);
       for (int it = 0; ok && it < w.n_it; ++it, ++g)
         ok = ew_step<LY, CAUSAL>(x, g, w.kt, w.i0 + it, Nk, off, window, c_log2, qw, h, lane, SITE_P_COMPUTE);
@@ -286,12 +298,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // released to the next unit
       if (!(ok = mbar_wait_warp(bar(B_DKVFULL), k & 1, x.guard, SITE_P_COMPUTE))) break;
       tc_fence_after();
-      uint32_t outp[D / 2];
       ew_load_dk_dv<D>(x, qw, h, scale, w.n_it == 0, outp);
       tc_fence_before();
       mbar_arrive(bar(B_DKVFREE));
-      const int key = w.kt * BN + qw * 32 + lane;
-      if (key < Nk) ew_store_dk_dv<D>(outp, dK, dV, static_cast<size_t>(w.bh) * Nk + key, h);
+      const int row0 = w.kt * BN + qw * 32;
+      prow0 = static_cast<size_t>(w.bh) * Nk + row0;
+      pvalid = Nk - row0;
+      pending = true;
     }
     }
   }

@@ -157,7 +157,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ---------------------------------------------------------------- element-wise warps
     const int qw = warp & 3;        // tensor-memory lane quarter
     const int h = (warp - 4) >> 2;  // query half (64 queries) of each tile
-    const int key = kt * BN + qw * 32 + lane;
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it)
       ok = ew_step<LY, CAUSAL>(x, it, kt, i0 + it, Nk, off, window, c_log2, qw, h, lane, SITE_COMPUTE);
@@ -167,7 +166,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_after();
       uint32_t outp[D / 2];
       ew_load_dk_dv<D>(x, qw, h, scale, n_it == 0, outp);
-      if (key < Nk) ew_store_dk_dv<D>(outp, dK, dV, krow0 + key, h);
+      const int row0 = kt * BN + qw * 32;
+      ew_store_dk_dv<D>(outp, dK, dV, krow0 + row0, Nk - row0, h, lane);
     }
     }
   }
