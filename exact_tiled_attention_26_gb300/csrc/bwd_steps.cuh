@@ -384,45 +384,14 @@ FA_DEV void ew_load_dk_dv(const Ctx& x, int qw, int h, float scale, bool none, u
 }
 
 // Second half: the warp's 32 key rows (rows row0 .. row0+31 of [B*H*Nk, D], the first
-// nvalid of them below Nk) into dK and dV.  Each lane holds its own row's NC 16-byte
-// chunks per tensor; a butterfly over groups of NC lanes hands lane i chunk i % NC of
-// the group's NC rows, so that each store instruction writes 32 / NC whole row halves
-// (D bytes each) instead of 32 scattered 16-byte pieces (half as many L2 sector
-// writes).  Every lane of the warp must call it.
+// nvalid of them below Nk) into dK and dV, d columns (D/2) h .. (D/2) h + D/2 - 1, with
+// whole-row writes.  Every lane of the warp must call it.
 template <int D>
 FA_DEV void ew_store_dk_dv(uint32_t (&outp)[D / 2], __nv_bfloat16* dK, __nv_bfloat16* dV, size_t row0, int nvalid,
                            int h, int lane) {
-  constexpr int HW = D / 2;   // d columns per query half
-  constexpr int NC = HW / 8;  // 16-byte chunks of a row half: 8 at d = 128, 4 at d = 64
-  constexpr int TW = HW / 2;  // words of one tensor's row half
-#pragma unroll
-  for (int m = NC / 2; m >= 1; m >>= 1) {
-    const bool hi = (lane & m) != 0;
-#pragma unroll
-    for (int t = 0; t < 2; ++t)
-#pragma unroll
-      for (int k0 = 0; k0 < NC; ++k0) {
-        if (k0 & m) continue;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          uint32_t& a0 = outp[TW * t + 4 * k0 + w];
-          uint32_t& a1 = outp[TW * t + 4 * (k0 | m) + w];
-          const uint32_t recv = __shfl_xor_sync(0xffffffffu, hi ? a0 : a1, m);
-          if (hi) a0 = recv; else a1 = recv;
-        }
-      }
-  }
-  const int c = lane & (NC - 1), g0 = lane & ~(NC - 1);
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    __nv_bfloat16* base = (t == 0 ? dK : dV) + HW * h + 8 * c;
-#pragma unroll
-    for (int j = 0; j < NC; ++j)
-      if (g0 + j < nvalid)
-        *reinterpret_cast<uint4*>(base + (row0 + g0 + j) * D) =
-            make_uint4(outp[TW * t + 4 * j], outp[TW * t + 4 * j + 1], outp[TW * t + 4 * j + 2],
-                       outp[TW * t + 4 * j + 3]);
-  }
+  constexpr int HW = D / 2;  // d columns per query half
+  warp_store_rows<HW / 8, 0>(outp, reinterpret_cast<uint8_t*>(dK + row0 * D + HW * h), D * 2, nvalid, lane);
+  warp_store_rows<HW / 8, HW / 2>(outp, reinterpret_cast<uint8_t*>(dV + row0 * D + HW * h), D * 2, nvalid, lane);
 }
 
 }  // namespace bsteps

@@ -215,8 +215,10 @@ __global__ void __launch_bounds__(256, 1)
     if (ok) ok = mbar_wait_warp(bar(C::B_OFINAL), 0, guard, SITE_FWD_SOFTMAX);
     if (ok) {
       tc_fence_after();
-      const size_t r0 = static_cast<size_t>(bh) * Nq + q;
-      softmax_epilogue<D>(st, tl + C::TM_O, O + r0 * D, Lout + r0, q < Nq);
+      uint32_t pk[D / 2];
+      softmax_epilogue_load<D>(st, tl + C::TM_O, pk);
+      const int w0 = qt * C::BM + wq * 32;  // the warp's first query row
+      softmax_epilogue_store_rows<D>(st, pk, O, Lout, static_cast<size_t>(bh) * Nq + w0, Nq - w0, lane);
     }
   }
 

@@ -232,8 +232,12 @@ __global__ void __launch_bounds__(PP::NTHREADS, 1)
       if (ok) ok = mbar_wait_warp(bar(C::B_PFREE + t), (n_t - 1) & 1, guard, SITE_PP_SOFTMAX);
       if (ok) {
         tc_fence_after();
-        const size_t r0 = static_cast<size_t>(bh) * Nq + q;
-        softmax_epilogue<D>(st, tO, O + r0 * D, Lout + r0, q < Nq);
+        uint32_t pk[D / 2];
+        softmax_epilogue_load<D>(st, tO, pk);
+        if (q < Nq) {
+          const size_t r0 = static_cast<size_t>(bh) * Nq + q;
+          softmax_epilogue_store<D>(st, pk, O + r0 * D, Lout + r0);
+        }
       }
     }
   }

@@ -128,31 +128,6 @@ FA_DEV bool softmax_tile(SoftmaxRow& st, uint32_t tS, uint32_t tO, bool first, i
   return true;
 }
 
-// Epilogue of one query row once every P V product into O (at tO) is complete:
-// O / l to bf16 (l = the sum of the very bf16 weights that entered P V, so that the
-// weights applied to V sum to one) and L = m + ln l with the unrounded sum.  Rows
-// at or past Nq compute but store nothing.
-template <int D>
-FA_DEV void softmax_epilogue(const SoftmaxRow& st, uint32_t tO, __nv_bfloat16* orow, float* lrow, bool store) {
-  const float inv_l = 1.f / st.lr_run;
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t o[32];
-    tmem_ld32(tO + 32 * c, o);
-    tmem_ld_wait<32>(o);
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-    if (store) {
-      uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-    }
-  }
-  if (store) *lrow = (st.m_run + lg2(st.l_run)) * kFwdLn2;
-}
-
 // The epilogue in two halves, for a caller that must release O's columns before the
 // global stores: load O / l into packed bf16 registers (the tensor-memory loads are
 // complete on return), then store them and L.
@@ -176,6 +151,16 @@ FA_DEV void softmax_epilogue_store(const SoftmaxRow& st, const uint32_t (&pk)[D 
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
   *lrow = (st.m_run + lg2(st.l_run)) * kFwdLn2;
+}
+
+// Second half for a whole warp: its 32 query rows (rows row0 .. row0+31 of [B*H*Nq, D],
+// the first nvalid of them below Nq) of O with whole-row writes, and this thread's L
+// (row row0 + lane, if below Nq).  Every lane of the warp must call it.
+template <int D>
+FA_DEV void softmax_epilogue_store_rows(const SoftmaxRow& st, uint32_t (&pk)[D / 2], __nv_bfloat16* O, float* Lout,
+                                        size_t row0, int nvalid, int lane) {
+  warp_store_rows<D / 8, 0>(pk, reinterpret_cast<uint8_t*>(O + row0 * D), D * 2, nvalid, lane);
+  if (lane < nvalid) Lout[row0 + lane] = (st.m_run + lg2(st.l_run)) * kFwdLn2;
 }
 
 }  // namespace fa

@@ -354,6 +354,38 @@ FA_DEV void add_bf16x2_f32(uint32_t pk, float& lo, float& hi) {
       : "r"(pk));
 }
 
+// Stores a warp's 32 rows with whole-row writes.  Lane l holds row l's NC 16-byte
+// chunks in words v[OFF .. OFF + 4 NC); row l goes to `base + l * stride` (bytes).  A
+// butterfly of shuffles over groups of NC lanes hands lane i chunk i % NC of its
+// group's NC rows, so that each store instruction writes 32 / NC whole rows of 16 NC
+// bytes instead of 32 scattered 16-byte pieces.  Only rows below nvalid are written.
+// Every lane of the warp must call it; v is left permuted.
+template <int NC, int OFF, int N>
+FA_DEV void warp_store_rows(uint32_t (&v)[N], uint8_t* base, size_t stride, int nvalid, int lane) {
+  static_assert(NC >= 1 && NC <= 32 && (NC & (NC - 1)) == 0 && OFF + 4 * NC <= N, "chunks");
+#pragma unroll
+  for (int m = NC / 2; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int k0 = 0; k0 < NC; ++k0) {
+      if (k0 & m) continue;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t& a0 = v[OFF + 4 * k0 + w];
+        uint32_t& a1 = v[OFF + 4 * (k0 | m) + w];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, hi ? a0 : a1, m);
+        if (hi) a0 = recv; else a1 = recv;
+      }
+    }
+  }
+  const int c = lane & (NC - 1), g0 = lane & ~(NC - 1);
+#pragma unroll
+  for (int j = 0; j < NC; ++j)
+    if (g0 + j < nvalid)
+      *reinterpret_cast<uint4*>(base + static_cast<size_t>(g0 + j) * stride + 16 * c) =
+          make_uint4(v[OFF + 4 * j], v[OFF + 4 * j + 1], v[OFF + 4 * j + 2], v[OFF + 4 * j + 3]);
+}
+
 // Programmatic dependent launch (a kernel launched with launch_pdl, internal.h, may
 // start while the kernel before it on the stream is still running).  pdl_wait:
 // block until that kernel has completed and its memory writes are visible (a no-op
