@@ -298,27 +298,19 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const uint32_t col = t == 0 ? C::TM_DK : C::TM_DV;
-        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (krow0 + key) * D;
+        const float f = t == 0 ? scale : 1.f;  // Eq 19's scale, applied once to dK
+        uint32_t r[32];
+        tmem_ld32(tl + col, r);
+        tmem_ld_wait<32>(r);
+        // the row as packed bf16 (zero when no query sees these keys: the accumulators
+        // were never written), then the warp's 32 rows with whole-row writes
+        uint32_t pk[D / 2];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tl + col + 32 * c, r);
-          tmem_ld_wait<32>(r);
-          const float f = t == 0 ? scale : 1.f;  // Eq 19's scale, applied once to dK
-          if (n_it == 0) {  // no query sees these keys: the accumulators were never written
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-          }
-          if (key < Nk) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * f, __uint_as_float(r[8 * i + 1]) * f),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 2]) * f, __uint_as_float(r[8 * i + 3]) * f),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 4]) * f, __uint_as_float(r[8 * i + 5]) * f),
-                                 pack_bf16x2(__uint_as_float(r[8 * i + 6]) * f, __uint_as_float(r[8 * i + 7]) * f));
-          }
-        }
+        for (int i = 0; i < D / 2; ++i)
+          pk[i] = n_it == 0 ? 0u : pack_bf16x2(__uint_as_float(r[2 * i]) * f, __uint_as_float(r[2 * i + 1]) * f);
+        const int w0 = kt * C::BN + wq * 32;  // the warp's first key row
+        warp_store_rows<D / 8, 0>(pk, reinterpret_cast<uint8_t*>((t == 0 ? dK : dV) + (krow0 + w0) * D), D * 2,
+                                  Nk - w0, lane);
       }
     }
   }

@@ -300,24 +300,19 @@ __global__ void __launch_bounds__(KVC<D>::NTHREADS, 1)
       for (int t = 0; t < 2; ++t) {
         const float f = t == 0 ? scale : 1.f;
         // this warp's D / 4 columns of d
-        __nv_bfloat16* dst = (t == 0 ? dK : dV) + (krow0 + key) * D + (D / 4) * qq;
         uint32_t r[32];
         if constexpr (D == 128) tmem_ld32(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 32 * qq, r);
         else tmem_ld16(tl + (t == 0 ? C::TM_DK : C::TM_DV) + 16 * qq, r);
         tmem_ld_wait<32>(r);
-        if (n_it == 0) {  // no query sees these keys: the accumulators were never written
+        // this warp's D / 4 columns of its 32 key rows, as packed bf16 (zero when no query
+        // sees these keys: the accumulators were never written)
+        uint32_t pk[D / 8];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
-        }
-        if (key < Nk) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-          for (int i = 0; i < D / 32; ++i)
-            d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * f, __uint_as_float(r[8 * i + 1]) * f),
-                               pack_bf16x2(__uint_as_float(r[8 * i + 2]) * f, __uint_as_float(r[8 * i + 3]) * f),
-                               pack_bf16x2(__uint_as_float(r[8 * i + 4]) * f, __uint_as_float(r[8 * i + 5]) * f),
-                               pack_bf16x2(__uint_as_float(r[8 * i + 6]) * f, __uint_as_float(r[8 * i + 7]) * f));
-        }
+        for (int i = 0; i < D / 8; ++i)
+          pk[i] = n_it == 0 ? 0u : pack_bf16x2(__uint_as_float(r[2 * i]) * f, __uint_as_float(r[2 * i + 1]) * f);
+        const int w0 = kt * 128 + qw * 32;  // the warp's first key row
+        warp_store_rows<D / 32, 0>(pk, reinterpret_cast<uint8_t*>((t == 0 ? dK : dV) + (krow0 + w0) * D + (D / 4) * qq),
+                                   D * 2, Nk - w0, lane);
       }
     }
   }
@@ -561,15 +556,13 @@ __global__ void __launch_bounds__(QC<D>::NTHREADS, 1)
       if constexpr (D == 128) tmem_ld32(tl + C::TM_DQ + 32 * kq, r);
       else tmem_ld16(tl + C::TM_DQ + 16 * kq, r);
       tmem_ld_wait<32>(r);
-      if (q < Nq) {
-        uint4* d4 = reinterpret_cast<uint4*>(dQ + (row0 + q) * D + (D / 4) * kq);
+      uint32_t pk[D / 8];
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i)
-          d4[i] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * i]) * scale, __uint_as_float(r[8 * i + 1]) * scale),
-                             pack_bf16x2(__uint_as_float(r[8 * i + 2]) * scale, __uint_as_float(r[8 * i + 3]) * scale),
-                             pack_bf16x2(__uint_as_float(r[8 * i + 4]) * scale, __uint_as_float(r[8 * i + 5]) * scale),
-                             pack_bf16x2(__uint_as_float(r[8 * i + 6]) * scale, __uint_as_float(r[8 * i + 7]) * scale));
-      }
+      for (int i = 0; i < D / 8; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]) * scale, __uint_as_float(r[2 * i + 1]) * scale);
+      const int w0 = qt * 128 + qw * 32;  // the warp's first query row
+      warp_store_rows<D / 32, 0>(pk, reinterpret_cast<uint8_t*>(dQ + (row0 + w0) * D + (D / 4) * kq), D * 2, Nq - w0,
+                                 lane);
     }
   }
   tc_fence_before();
