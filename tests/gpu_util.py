@@ -71,11 +71,13 @@ def lib():
     return fa
 
 
-def run_gpu(Q, K, V, dO, causal, scale=None, counter=False, split=0, window=0):
+def run_gpu(Q, K, V, dO, causal, scale=None, counter=False, split=0, window=0, ws=None):
     """Forward + preprocess + backward through the C ABI (the general-mask entry
     points).  Inputs: bf16 CPU tensors Q, dO [B,H,Nq,d], K, V [B,H,Nk,d].  `split`
     selects the backward form (fa_debug_set_bwd_split; 0 = the library's default).
-    Returns CPU tensors and (if asked) the tile-pair counts."""
+    `ws`: a device uint8 tensor to use as the backward's workspace, with whatever it
+    holds (default: a new one).  Returns CPU tensors and (if asked) the tile-pair
+    counts."""
     fa = lib()
     fa.check(fa.fa_debug_set_bwd_split(split))
     B, H, Nq, d = Q.shape
@@ -88,7 +90,9 @@ def run_gpu(Q, K, V, dO, causal, scale=None, counter=False, split=0, window=0):
     D = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws_bytes = fa.fa_bwd_workspace_size_ex(B, H, Nq, Nk, d, causal, window)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    if ws is None:
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    assert ws.numel() >= ws_bytes
     cnt = torch.zeros(2, dtype=torch.int64, device=dev)
     s = stream()
     if counter:

@@ -51,6 +51,23 @@ def test_large_logits_and_scale(d, split, causal):
     assert_close(_grads(got), {n: ref[n] for n in ("dQ", "dK", "dV")}, f"split={split} qk x4")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("split", [1, 3])
+@pytest.mark.parametrize("causal", [False, True])
+def test_workspace_content_on_entry_does_not_matter(d, split, causal):
+    """The one-kernel forms reduce dQ into the fp32 workspace, which the call clears
+    first: a workspace full of NaN bit patterns, then the same workspace as the
+    first call left it, give the oracle's gradients for two different problems
+    (ragged length, three heads)."""
+    ws = torch.full((8 << 20,), 0xFF, dtype=torch.uint8, device="cuda")
+    for seed in (61, 62):
+        Q, K, V, dO = si.make_qkvdo(1, 3, 300, d, seed=seed + d)
+        got = run_gpu(Q, K, V, dO, causal, split=split, ws=ws)
+        ref = _oracle_full(Q, K, V, dO, causal)
+        assert_close(_grads(got), {n: ref[n] for n in ("dQ", "dK", "dV")},
+                     f"d={d} split={split} causal={causal} seed={seed}")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_mid_workload_sampled_rows_form2(causal):
     """The mid workload (2 x 16 heads x 4096 x 128) through form 2: dQ on sampled
