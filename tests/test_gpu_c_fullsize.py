@@ -11,6 +11,7 @@ checks:
 """
 import numpy as np
 import pytest
+import torch
 
 import oracle
 import seeded_inputs as si
@@ -116,3 +117,28 @@ def test_tile_pairs_exact(name, causal):
     if causal and w.N % 128 == 0:
         T = w.N // 128
         assert fwd == w.B * w.H * T * (T + 1) // 2
+
+
+def test_one_head_of_131072_rows():
+    """One head of 131072 rows at d = 64, causal: 1024 query and key tiles, the
+    largest tile and unit indices of any test.  O, L, dQ and D on 64 sampled rows
+    (the first and last among them) against the oracle; dK and dV of the persistent
+    backward bit-identical to the two-kernel backward's (the same bf16 P^T and dS^T,
+    summed in the same order).  dQ of the two is summed in different orders over up
+    to 1024 key tiles (in tensor memory, against fp32 reductions in L2); the fp32
+    sums differ by ~1e-5 and flip the bf16 rounding of a fraction of a percent of
+    the elements (2.9e-4 relative Frobenius measured), while one key tile's
+    contribution missing or counted twice would move it by far more than 2e-3."""
+    N, d = 131072, 64
+    Q, K, V, dO = si.make_qkvdo(1, 1, N, d, seed=91)
+    a = run_gpu(Q, K, V, dO, True, split=3)
+    b = run_gpu(Q, K, V, dO, True, split=2)
+    rng = np.random.default_rng(92)
+    rows = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 62, replace=False)]))
+    q, k, v, do = (f64(t.reshape(1, N, d)) for t in (Q, K, V, dO))
+    O, L, dQ, D = oracle.rows_fwd_bwd(q, k, v, do, rows, True)
+    g = {n: f64(a[n].reshape(1, N, d) if a[n].dim() == 4 else a[n].reshape(1, N))[:, rows]
+         for n in ("O", "L", "dQ", "D")}
+    assert_close(g, {"O": O, "L": L, "dQ": dQ, "D": D}, "1x1x131072x64 causal rows")
+    assert torch.equal(a["dK"], b["dK"]) and torch.equal(a["dV"], b["dV"])
+    assert rel_frob(f64(a["dQ"]), f64(b["dQ"])) < 2e-3
