@@ -85,3 +85,29 @@ def test_repeat_calls_are_deterministic_in_O_and_L():
     b = run_gpu(Q, K, V, dO, True)
     assert (a["O"] == b["O"]).all() and (a["L"] == b["L"]).all()
     assert (a["dK"] == b["dK"]).all() and (a["dV"] == b["dV"]).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_d32_multi_tile_multi_head(causal):
+    """d = 32 (its own one-kernel backward) at 32 query and key tiles per head and
+    four heads, against the full oracle, with exact tile counts."""
+    B, H, N, d = 2, 2, 4096, 32
+    Q, K, V, dO = si.make_qkvdo(B, H, N, d, seed=71)
+    got = run_gpu(Q, K, V, dO, causal, counter=True)
+    ref = _oracle_full(Q, K, V, dO, causal)
+    assert_close({n: f64(t) for n, t in got.items() if n != "tiles"}, ref, f"2x2x4096x32 causal={causal}")
+    _check_counts(got, B, H, N, d, causal)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_heads_of_short_sequences(d, causal):
+    """256 heads of 384 rows (3 tiles each): every head in one launch group, 768
+    short units for the persistent kernels' queues, ragged-free but many boundaries;
+    every output against the full oracle, with exact tile counts."""
+    B, H, N = 8, 32, 384
+    Q, K, V, dO = si.make_qkvdo(B, H, N, d, seed=72 + d)
+    got = run_gpu(Q, K, V, dO, causal, counter=True)
+    ref = _oracle_full(Q, K, V, dO, causal)
+    assert_close({n: f64(t) for n, t in got.items() if n != "tiles"}, ref, f"8x32x384x{d} causal={causal}")
+    _check_counts(got, B, H, N, d, causal)
