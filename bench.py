@@ -162,9 +162,12 @@ class Runner:
         lo = np.maximum(0, i + off - self.window + 1) if self.window > 0 else np.zeros_like(i)
         return int((hi - lo + 1).sum())
 
-    # kernels this library launches per step: fwd, preprocess, bwd main, dQ convert
-    # (or, with the two-kernel backward: fwd, preprocess, key-tile kernel, query-tile kernel)
-    LAUNCHES_PER_STEP = 4
+    @staticmethod
+    def launches_per_step(bwd_form):
+        """Kernels this library launches per step: the forward, the preprocess, then with a
+        one-kernel backward (forms 1, 3) the workspace clear, the backward kernel and the dQ
+        convert, or with the two-kernel backward (form 2) its key-tile and query-tile kernels."""
+        return 4 if bwd_form == 2 else 5
 
 
 def time_steps(torch, r: Runner, steps: int, warmup: int, flush=None, kernel_events=False):
@@ -387,7 +390,7 @@ def run_ours(args):
             "algorithmic": "10 N^2 d / 2 FLOPs per head (causal) per launch",
             "frac_of_sustained": round(bwd_kernel_tflops / sustained, 4),
         },
-        "gpu_launches": Runner.LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": Runner.launches_per_step(b_form) * args.steps,
         "clocks": clocks,
     }
     if args.window:
